@@ -1,0 +1,218 @@
+"""CPU oracle for context-parallel attention: plain, slow and meant to be obviously correct.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import this module: only the test
+suite, ``__graft_entry__.smoke()`` and the CPU-baseline legs of ``bench.py`` use it.  It shares
+no code, table or helper with the CUDA library; both sides only share the seeded input drawer.
+
+All arithmetic is float64 numpy.  16-bit inputs are converted to float64 exactly before use.
+
+Every function follows a passage of "Scaling AI Inference Across Multiple GPUs Using NVIDIA
+TensorRT with Multi-Device Inference Support" (the primary page), section "Parallelism
+strategies for distributed inference":
+
+* ``attention`` -- subsection "Context parallelism": the bidirectional (non-causal) attention
+  of a diffusion transformer over the whole sequence.  The page gives no formula; the reading
+  used is softmax(Q K^T * scale) V with scale = 1/sqrt(D), and LSE is the natural logarithm of
+  the softmax denominator sum_j exp(scale * q.k_j).  The result is written straight from that
+  definition (the usual max shift is applied before exp, which changes no value, only avoids
+  overflow).
+* ``attention_chunked`` -- subsection "Ring Attention" and Figure 3: each rank holds one slice
+  of K and V; the slice attended by a query tile produces a partial output.  Partial c is the
+  plain definition restricted to KV rows [floor(c*Skv/P), floor((c+1)*Skv/P)), normalised over
+  that slice only, with its own LSE.
+* ``attention_online`` -- subsection "Ring Attention": "online softmax" so that the full-size K
+  and V are never materialised.  The running max m, running sum l and running accumulator are
+  updated block by block, in the order the blocks arrive.
+* ``lse_merge`` -- subsection "Ring Attention" (the attention output is updated as KV blocks
+  stream past): combine per-chunk partials by their log-sum-exp weights.
+* ``seq2head`` / ``head2seq`` -- subsection "DeepSpeed Ulysses" and Figure 4: the first
+  all-to-all turns sequence sharding into head sharding (every rank ends with the full sequence
+  for a disjoint subset of heads), the second turns it back.
+"""
+from __future__ import annotations
+
+import math
+from typing import Tuple
+
+import numpy as np
+
+__all__ = ["to_f64", "attention", "chunk_bounds", "attention_chunked", "attention_online",
+           "lse_merge", "seq2head", "head2seq", "softmax_weights"]
+
+# Query rows processed at once.  Rows are independent in the definition, so this only bounds
+# the size of the temporary score matrix; it does not reorder any reduction.
+_ROW_BLOCK_BYTES = 192 << 20
+
+
+def to_f64(x) -> np.ndarray:
+    """Exact conversion of a torch tensor (bf16 / fp16 / fp32 / fp64) or array to float64."""
+    if hasattr(x, "detach"):
+        import torch  # local: only for dtype conversion of inputs
+        return x.detach().to("cpu", torch.float64).numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def _default_scale(D: int) -> float:
+    return 1.0 / math.sqrt(D)
+
+
+def softmax_weights(q, k, scale: float | None = None) -> np.ndarray:
+    """The attention weight matrix softmax(q k^T * scale) for one head: q [Sq, D], k [Skv, D]."""
+    q = to_f64(q)
+    k = to_f64(k)
+    if scale is None:
+        scale = _default_scale(q.shape[-1])
+    s = (q @ k.T) * scale
+    s = s - s.max(axis=1, keepdims=True)
+    e = np.exp(s)
+    return e / e.sum(axis=1, keepdims=True)
+
+
+def _attention_head(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float):
+    """One (batch, head): q [Sq, D], k/v [Skv, D] -> (o [Sq, D], lse [Sq])."""
+    Sq = q.shape[0]
+    Skv = k.shape[0]
+    o = np.empty((Sq, v.shape[1]), dtype=np.float64)
+    lse = np.empty((Sq,), dtype=np.float64)
+    rows = max(1, _ROW_BLOCK_BYTES // max(1, 8 * Skv))
+    for r0 in range(0, Sq, rows):
+        r1 = min(Sq, r0 + rows)
+        s = (q[r0:r1] @ k.T) * scale               # logits s_ij = scale * q_i . k_j
+        m = s.max(axis=1, keepdims=True)            # shift only; exp(s - m) / sum is unchanged
+        e = np.exp(s - m)
+        denom = e.sum(axis=1, keepdims=True)
+        o[r0:r1] = (e @ v) / denom                  # O_i = sum_j softmax_ij v_j
+        lse[r0:r1] = (m + np.log(denom))[:, 0]      # ln sum_j exp(s_ij)
+    return o, lse
+
+
+def attention(q, k, v, scale: float | None = None) -> Tuple[np.ndarray, np.ndarray]:
+    """Non-causal multi-head attention.
+
+    q: [..., Sq, D], k and v: [..., Skv, D] (any leading batch/head dims, equal for all three).
+    Returns (O [..., Sq, D], LSE [..., Sq]) in float64.
+    """
+    q = to_f64(q)
+    k = to_f64(k)
+    v = to_f64(v)
+    if scale is None:
+        scale = _default_scale(q.shape[-1])
+    lead = q.shape[:-2]
+    assert k.shape[:-2] == lead and v.shape[:-2] == lead
+    qf = q.reshape((-1,) + q.shape[-2:])
+    kf = k.reshape((-1,) + k.shape[-2:])
+    vf = v.reshape((-1,) + v.shape[-2:])
+    o = np.empty(qf.shape[:-1] + (vf.shape[-1],), dtype=np.float64)
+    lse = np.empty(qf.shape[:-1], dtype=np.float64)
+    for i in range(qf.shape[0]):
+        o[i], lse[i] = _attention_head(qf[i], kf[i], vf[i], scale)
+    return o.reshape(lead + o.shape[-2:]), lse.reshape(lead + lse.shape[-1:])
+
+
+def chunk_bounds(Skv: int, P: int, c: int) -> Tuple[int, int]:
+    """KV rows [lo, hi) of chunk c out of P: contiguous slices, balanced by a floor split, as a
+    ring rank c that holds sequence slice c would see them."""
+    return (c * Skv) // P, ((c + 1) * Skv) // P
+
+
+def attention_chunked(q, k, v, P: int, scale: float | None = None):
+    """Per-chunk partial outputs of attention over KV split into P contiguous chunks.
+
+    Returns (O_parts [P, ..., Sq, D], LSE_parts [P, ..., Sq]); partial c is the attention of q
+    over KV rows chunk_bounds(Skv, P, c) only, normalised over those rows.
+    """
+    q = to_f64(q)
+    k = to_f64(k)
+    v = to_f64(v)
+    Skv = k.shape[-2]
+    assert 1 <= P <= Skv
+    outs, lses = [], []
+    for c in range(P):
+        lo, hi = chunk_bounds(Skv, P, c)
+        o_c, lse_c = attention(q, k[..., lo:hi, :], v[..., lo:hi, :], scale)
+        outs.append(o_c)
+        lses.append(lse_c)
+    return np.stack(outs), np.stack(lses)
+
+
+def attention_online(q, k, v, block: int = 128, scale: float | None = None):
+    """Online-softmax attention: visit KV in blocks of ``block`` rows, in order, keeping per query
+    row a running max m, running denominator l and running (unnormalised) accumulator acc.
+
+    For each block with logits s:  m' = max(m, max_j s_j);  l = l * exp(m - m') + sum_j exp(s_j - m');
+    acc = acc * exp(m - m') + sum_j exp(s_j - m') v_j;  m = m'.
+    At the end O = acc / l and LSE = m + ln l.
+    """
+    q = to_f64(q)
+    k = to_f64(k)
+    v = to_f64(v)
+    if scale is None:
+        scale = _default_scale(q.shape[-1])
+    Skv = k.shape[-2]
+    m = np.full(q.shape[:-1], -np.inf)
+    l = np.zeros(q.shape[:-1])
+    acc = np.zeros(q.shape[:-1] + (v.shape[-1],))
+    for j0 in range(0, Skv, block):
+        kb = k[..., j0:j0 + block, :]
+        vb = v[..., j0:j0 + block, :]
+        s = np.einsum("...id,...jd->...ij", q, kb) * scale
+        m_new = np.maximum(m, s.max(axis=-1))
+        corr = np.exp(m - m_new)                    # exp(-inf) = 0 on the first block
+        e = np.exp(s - m_new[..., None])
+        l = l * corr + e.sum(axis=-1)
+        acc = acc * corr[..., None] + np.einsum("...ij,...jd->...id", e, vb)
+        m = m_new
+    return acc / l[..., None], m + np.log(l)
+
+
+def lse_merge(o_parts, lse_parts):
+    """Merge P partial attention outputs by their log-sum-exp weights.
+
+    o_parts [P, ..., D], lse_parts [P, ...].  With M = max_c LSE_c, w_c = exp(LSE_c - M):
+    LSE = M + ln sum_c w_c  and  O = sum_c w_c O_c / sum_c w_c.
+    Rows whose partials all have LSE = -inf (no KV rows at all) merge to O = 0, LSE = -inf.
+    """
+    o = to_f64(o_parts)
+    lse = to_f64(lse_parts)
+    M = lse.max(axis=0)
+    finite = np.isfinite(M)
+    Ms = np.where(finite, M, 0.0)
+    w = np.where(finite[None], np.exp(lse - Ms[None]), 0.0)
+    W = w.sum(axis=0)
+    Wsafe = np.where(finite, W, 1.0)
+    out = (w[..., None] * o).sum(axis=0) / Wsafe[..., None]
+    out = np.where(finite[..., None], out, 0.0)
+    lse_out = np.where(finite, Ms + np.log(Wsafe), -np.inf)
+    return out, lse_out
+
+
+def seq2head(x, P: int) -> np.ndarray:
+    """First Ulysses all-to-all, emulated on one device.
+
+    Input [P][B][S/P][H][D]: rank p holds tokens p*S/P .. (p+1)*S/P - 1 for all H heads.
+    Output [P][B][H/P][S][D]: rank g holds all S tokens, in global order, for heads
+    g*H/P .. (g+1)*H/P - 1.  Element map: out[g][b][j][p*S/P + s][d] = in[p][b][s][g*H/P + j][d].
+    Pure data movement: works on any dtype and returns the same dtype.
+    """
+    x = np.asarray(x)
+    Pi, B, Sl, H, D = x.shape
+    assert Pi == P and H % P == 0
+    Hl = H // P
+    y = x.reshape(P, B, Sl, P, Hl, D)          # [p][b][s][g][j][d]
+    y = y.transpose(3, 1, 4, 0, 2, 5)          # [g][b][j][p][s][d]
+    return np.ascontiguousarray(y.reshape(P, B, Hl, P * Sl, D))
+
+
+def head2seq(y, P: int) -> np.ndarray:
+    """Second Ulysses all-to-all: the exact inverse of ``seq2head``.
+
+    Input [P][B][H/P][S][D] -> output [P][B][S/P][H][D],
+    out[p][b][s][g*H/P + j][d] = in[g][b][j][p*S/P + s][d].
+    """
+    y = np.asarray(y)
+    Pg, B, Hl, S, D = y.shape
+    assert Pg == P and S % P == 0
+    Sl = S // P
+    x = y.reshape(P, B, Hl, P, Sl, D)          # [g][b][j][p][s][d]
+    x = x.transpose(3, 1, 4, 0, 2, 5)          # [p][b][s][g][j][d]
+    return np.ascontiguousarray(x.reshape(P, B, Sl, P * Hl, D))
