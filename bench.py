@@ -1,0 +1,429 @@
+"""Benchmark of the context-parallel attention path on B300.
+
+One step = the ring-emulation hot path on the video-DiT workload (B=1, H=16, S=44,160, D=128,
+bf16): attn_fwd_chunked over P=8 KV chunks, then attn_lse_merge of the eight partials.  The
+metric is attention TFLOP/s = 4*B*H*Sq*Skv*D per step / step time.  Extra legs report the
+attention kernel alone against the tensor-core roofline, the merge and Ulysses layout kernels in
+GB/s against HBM, an end-to-end number through the same API with host buffers, and the CPU
+oracle timed on a bounded sample.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+                    [--no-cpu-baseline] [--no-e2e]
+
+Prints one JSON line (rank 0).  With torchrun each rank runs an independent replica of the same
+workload on its own GPU (the path needs no exchange on one box); ``value`` is the sum over ranks
+divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from context_math_non_b300.inputs import WORKLOADS, draw_qkv  # noqa: E402
+
+WORKLOAD = WORKLOADS["video"]
+P_CHUNKS = 8
+METRIC = "attention fwd TFLOP/s (4*B*H*Sq*Skv*D per step; KV in P=8 chunks + LSE merge)"
+UNIT = "TFLOP/s"
+CONFIG = {
+    "workload": "video-DiT long sequence: B=1 H=16 S=44160 D=128 bf16 N(0,1), non-causal, "
+                "KV split into P=8 chunks (per-chunk O + LSE), then LSE merge",
+    "B": 1, "H": 16, "S": 44160, "D": 128, "P": P_CHUNKS,
+    "l2": "no flush: every input is larger than L2 (Q/K/V 181 MB each, partials 1.45 GB)",
+    "parallelism": "replicas",
+}
+ATTN_SOURCES = ["context_math_non_b300/csrc/attn_fwd_sm103.cu",
+                "context_math_non_b300/csrc/ptx_sm103.cuh"]
+
+
+def _dist():
+    if "RANK" in os.environ and "WORLD_SIZE" in os.environ and int(os.environ["WORLD_SIZE"]) > 1:
+        return int(os.environ["RANK"]), int(os.environ["WORLD_SIZE"]), int(
+            os.environ.get("LOCAL_RANK", 0))
+    return 0, 1, 0
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16": d["bf16_tflops"],
+                "bf16_sustained": d["bf16_tflops_sustained"], "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6400.0, "bf16": 1800.0, "bf16_sustained": 1400.0, "source": "fallback"}
+
+
+def _src_hash() -> str:
+    h = hashlib.sha256()
+    for p in ATTN_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic():
+    """DRAM bytes per attention launch from the committed ncu summary, if it was taken on the
+    current kernel source (else None)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "attn_fwd_traffic.json")) as f:
+            d = json.load(f)
+        if d.get("kernel_source_sha") == _src_hash():
+            return d["bytes_per_launch_full_size"]
+    except (OSError, KeyError, ValueError):
+        pass
+    return None
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons with nvidia-smi while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        sm, mx = [], None
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[2:]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- native arm
+
+def run_native(args, rank, world, local_rank):
+    from context_math_non_b300 import cpattn
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = WORKLOAD
+    q, k, v = draw_qkv(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    B, H, S, D = w.B, w.H, w.S, w.D
+    op = torch.empty((P_CHUNKS, B, H, S, D), dtype=w.dtype, device=dev)
+    lp = torch.empty((P_CHUNKS, B, H, S), dtype=torch.float32, device=dev)
+    o = torch.empty((B, H, S, D), dtype=w.dtype, device=dev)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flops = w.attention_flops()
+    merge_bytes = (P_CHUNKS + 1) * B * H * S * (D * 2 + 4)
+
+    def step():
+        cpattn.attn_fwd_chunked(qd, kd, vd, P_CHUNKS, op, lp, stream=stream)
+        cpattn.attn_lse_merge(op, lp, o, lse, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    st = cpattn.attn_device_status(stream)
+    if st != cpattn.ATTN_OK:
+        raise RuntimeError(f"device status after warm-up: {cpattn.attn_status_string(st)}")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clocks:
+        t_start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            cpattn.attn_fwd_chunked(qd, kd, vd, P_CHUNKS, op, lp, stream=stream)
+            ev[i][1].record(stream)
+            cpattn.attn_lse_merge(op, lp, o, lse, stream=stream)
+            ev[i][2].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    attn_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    merge_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    st = cpattn.attn_device_status(stream)
+    if st != cpattn.ATTN_OK:
+        raise RuntimeError(f"device status after timing: {cpattn.attn_status_string(st)}")
+
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+
+    peaks = _peaks()
+    attn_avg = sum(attn_ms) / len(attn_ms)
+    achieved = flops / (attn_avg * 1e-3) / 1e12
+    merge_avg = sum(merge_ms) / len(merge_ms)
+    roofline = {
+        "kernel": "attn_fwd_kernel<128,bf16> (attn_fwd_chunked, P=8)",
+        "bound": "tensor", "achieved": round(achieved, 2),
+        "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
+        "frac": round(achieved / peaks["bf16_sustained"], 4),
+        "peak_note": f"{peaks['source']} sustained dense bf16 (kernel timed inside a long step); "
+                     f"frac of {peaks['source']} burst peak {peaks['bf16']}: "
+                     f"{achieved / peaks['bf16']:.4f}",
+        "avg_launch_ms": round(attn_avg, 4),
+        "traffic": _traffic(),
+        "algorithmic_flops_per_launch": flops,
+    }
+    legs = {
+        "lse_merge": {"avg_ms": round(merge_avg, 4), "bytes": merge_bytes,
+                      "GB/s": round(merge_bytes / (merge_avg * 1e-3) / 1e9, 1),
+                      "frac_of_hbm": round(merge_bytes / (merge_avg * 1e-3) / 1e9 /
+                                           peaks["hbm_gbs"], 4)},
+    }
+    legs.update(_layout_leg(cpattn, dev, stream, peaks))
+    clk = clocks.summary()
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = _e2e_leg(cpattn, q, k, v, dev, stream, args, flops, world)
+    del op, lp, qd, kd, vd
+    torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(q, k, v, budget_s=args.cpu_seconds)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) bf16 draws of the video-DiT shape",
+        "config": CONFIG, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": 2 * args.steps, "clocks": clk, "legs": legs,
+    }
+    return line
+
+
+def _layout_leg(cpattn, dev, stream, peaks, iters=10):
+    """Ulysses seq2head on the Ulysses workload shape ([8][2][2048][32][64] fp16, 134 MB):
+    the buffers are rotated over 4 sets (1.07 GB) so no iteration reads from L2."""
+    w = WORKLOADS["ulysses"]
+    P, B, S, H, D = w.P[0], w.B, w.S, w.H, w.D
+    nbytes = P * B * (S // P) * H * D * 2
+    sets = [(torch.empty((P, B, S // P, H, D), dtype=torch.float16, device=dev).normal_(),
+             torch.empty((P, B, H // P, S, D), dtype=torch.float16, device=dev))
+            for _ in range(4)]
+    for x, y in sets:
+        cpattn.cp_layout_seq2head(x, y, stream=stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(iters)]
+    for i in range(iters):
+        x, y = sets[i % 4]
+        evs[i][0].record(stream)
+        cpattn.cp_layout_seq2head(x, y, stream=stream)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+    gbs = 2 * nbytes / (ms * 1e-3) / 1e9
+    del sets
+    return {"cp_layout_seq2head": {"median_ms": round(ms, 4), "bytes": 2 * nbytes,
+                                   "GB/s": round(gbs, 1),
+                                   "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}}
+
+
+def _e2e_leg(cpattn, q, k, v, dev, stream, args, flops, world):
+    """Same step through the same API, but inputs start in pinned host memory and the merged
+    O and LSE are read back to pinned host memory every step (copies inside the timed region)."""
+    w = WORKLOAD
+    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+    dq, dk, dv = (torch.empty_like(t, device=dev) for t in (q, k, v))
+    op = torch.empty((P_CHUNKS, w.B, w.H, w.S, w.D), dtype=w.dtype, device=dev)
+    lp = torch.empty((P_CHUNKS, w.B, w.H, w.S), dtype=torch.float32, device=dev)
+    o = torch.empty((w.B, w.H, w.S, w.D), dtype=w.dtype, device=dev)
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        cpattn.attn_fwd_chunked(dq, dk, dv, P_CHUNKS, op, lp, stream=stream)
+        cpattn.attn_lse_merge(op, lp, o, lse, stream=stream)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    steps = max(1, args.steps // 2)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
+    d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+    return {"value": round(world * flops * steps / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": round(ms / steps, 3)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def _oracle_sample(q, k, v, rows_per_head: int, heads: int):
+    """Oracle chunked attention (P=8) + merge for the first rows of the first heads."""
+    import oracle
+    qs = q[:, :heads, :rows_per_head]
+    op, lp = oracle.attention_chunked(qs, k[:, :heads], v[:, :heads], P_CHUNKS)
+    return oracle.lse_merge(op, lp)
+
+
+def _blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d["num_threads"] for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:  # noqa: BLE001 - informational only
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(q, k, v, budget_s: float = 15.0):
+    """The float64 oracle, as it stands, timed on this host on a bounded sample of the same
+    workload: R query rows of every head through chunked attention (P=8) and the merge."""
+    w = WORKLOAD
+    t0 = time.perf_counter()
+    _oracle_sample(q, k, v, 32, 1)                  # calibration (also warms BLAS)
+    t_cal = time.perf_counter() - t0
+    per_row = t_cal / 32
+    rows = int(max(16, min(w.S, budget_s / per_row / w.H)))
+    t0 = time.perf_counter()
+    _oracle_sample(q, k, v, rows, w.H)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * w.B * w.H * rows * w.S * w.D
+    return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": _blas_threads(),
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"first {rows} query rows of each of the {w.H} heads (of {w.S}), full KV, "
+                      f"P=8 chunks + merge, float64 numpy"}
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle as it stands, one bounded sample per step."""
+    w = WORKLOAD
+    q, k, v = draw_qkv(w)
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        _oracle_sample(q, k, v, rows, w.H)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_sample(q, k, v, rows, w.H)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * w.B * w.H * rows * w.S * w.D * args.steps
+    value = flops / dt / 1e12
+    sample = (f"each step: first {rows} query rows of each of the {w.H} heads (of {w.S}), full KV,"
+              f" P=8 chunks + merge, float64 numpy")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": CONFIG,
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": _blas_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-rows", type=int, default=24)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local_rank = _dist()
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        line = run_native(args, rank, world, local_rank)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

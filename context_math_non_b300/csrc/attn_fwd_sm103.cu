@@ -1,0 +1,545 @@
+// Non-causal attention forward on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// Computes, for every query row, the attention over one contiguous KV range -- the whole
+// sequence (P = 1) or one of P chunks, each chunk standing in for one step of Ring Attention
+// ("Scaling AI Inference Across Multiple GPUs Using NVIDIA TensorRT with Multi-Device Inference
+// Support", subsection "Ring Attention", Figure 3) -- with an online softmax, so the full score
+// matrix never exists anywhere.  Outputs: O normalised over the range, and the range's
+// natural-log LSE.
+//
+// Work unit: (chunk c, batch*head bh, 256-query block qb).  A persistent grid of one CTA per SM
+// walks the units in a static round-robin; consecutive units share (bh, c), so the CTAs resident
+// at one time read the same K/V chunk and L2 serves the re-reads.
+//
+// CTA roles (384 threads = 3 warpgroups):
+//   warps 0-3  softmax for query tile 0 (thread = row; TMEM lanes 0..127)
+//   warps 4-7  softmax for query tile 1
+//   warp  8    TMA producer: Q tiles once per unit, then K_j / V_j through a ring of stages
+//   warp  9    TMEM allocation and the single MMA-issuing thread
+//   warps 10-11 idle (they complete the third warpgroup)
+// Tensor memory (512 columns): S0 | S1 | O0 | O1.  P (16-bit) is written over the first half of
+// its S columns and read from TMEM by the P*V MMA.  The MMA order per KV step j
+//   O0 += P0 V_{j-1};  S0 = Q0 K_j^T;  O1 += P1 V_{j-1};  S1 = Q1 K_j^T
+// lets each softmax warpgroup work on its tile while the tensor core runs the other tile's two
+// GEMMs.  The running max is only moved (and O rescaled) when it grows by more than 2^8, so most
+// steps skip the rescale; the final normalisation uses the same stale max, so results are exact.
+//
+// Every wait is bounded (see mbar_wait): a lost signal ends the kernel with ATTN_ERR_TIMEOUT in
+// the status word instead of a hang.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "cpattn_internal.h"
+#include "ptx_sm103.cuh"
+
+namespace cpattn {
+
+__device__ int g_attn_status = 0;
+
+namespace {
+
+constexpr int kBM = 128;          // query rows per tile (= TMEM lanes)
+constexpr int kBN = 128;          // KV rows per tile
+constexpr int kQT = 2;            // query tiles per CTA
+constexpr int kHalfBytes = 128 * 128;  // [128 rows][64 x 16-bit] swizzled box = 16 KB
+constexpr int kThreads = 384;
+
+constexpr int kLoaderWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct Cfg {
+  static constexpr int NH = D / 64;                       // 64-wide halves per row
+  static constexpr int TILE = NH * kHalfBytes;            // bytes of one 128-row tile
+  static constexpr int STAGES = (D == 128) ? 5 : 8;       // K/V ring depth
+  static constexpr int NBARS = 2 * STAGES + 8 * kQT + 1;
+  static constexpr int SMEM = 1024 /*alignment slack*/ + kQT * TILE + STAGES * TILE +
+                              NBARS * 8 + 16;
+  static constexpr uint32_t S_COL0 = 0, S_COL1 = 128, O_COL0 = 256, O_COL1 = 256 + D;
+};
+
+struct Params {
+  int Sq, Skv, P, BH, n_qb;
+  long long num_units;
+  float scale_log2;
+  void* o;      // [P][BH][Sq][D]
+  float* lse;   // [P][BH][Sq] or null
+  unsigned long long limit_ns;
+};
+
+struct Unit {
+  int qb, c, bh, lo, n, last_valid;
+};
+
+__device__ __forceinline__ Unit decode_unit(long long u, const Params& p) {
+  Unit w;
+  w.qb = static_cast<int>(u % p.n_qb);
+  long long r = u / p.n_qb;
+  w.c = static_cast<int>(r % p.P);
+  w.bh = static_cast<int>(r / p.P);
+  const long long lo = static_cast<long long>(w.c) * p.Skv / p.P;
+  const long long hi = static_cast<long long>(w.c + 1) * p.Skv / p.P;
+  const int len = static_cast<int>(hi - lo);
+  w.lo = static_cast<int>(lo);
+  w.n = (len + kBN - 1) / kBN;
+  w.last_valid = len - (w.n - 1) * kBN;
+  return w;
+}
+
+// Wait for an already-issued asynchronous completion regardless of the abort flag (used only to
+// drain in-flight copies / MMAs before the CTA exits on the error path).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer_ns() - t0 > limit_ns) return;
+  }
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + kQT * C::TILE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + C::STAGES * C::TILE);
+  uint64_t* kv_full = bars;
+  uint64_t* kv_empty = bars + C::STAGES;
+  uint64_t* q_full = bars + 2 * C::STAGES;
+  uint64_t* q_empty = q_full + kQT;
+  uint64_t* s_full = q_empty + kQT;
+  uint64_t* p_full = s_full + kQT;
+  uint64_t* o_full = p_full + kQT;
+  uint64_t* o_empty = o_full + kQT;
+  uint64_t* mma_drain = o_empty + kQT;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint64_t lim = p.limit_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      ptx::mbar_init(&kv_full[s], 1);
+      ptx::mbar_init(&kv_empty[s], 1);
+    }
+    for (int t = 0; t < kQT; ++t) {
+      ptx::mbar_init(&q_full[t], 1);
+      ptx::mbar_init(&q_empty[t], 1);
+      ptx::mbar_init(&s_full[t], 1);
+      ptx::mbar_init(&p_full[t], 4);
+      ptx::mbar_init(&o_full[t], 1);
+      ptx::mbar_init(&o_empty[t], 4);
+    }
+    ptx::mbar_init(mma_drain, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(tmem_slot, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp == kLoaderWarp && lane == 0) {
+    ptx::prefetch_tmap(&tm_q);
+    ptx::prefetch_tmap(&tm_k);
+    ptx::prefetch_tmap(&tm_v);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kLoaderWarp) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t kv_pos = 0, it = 0;
+      int q_issued[kQT];
+      for (int t = 0; t < kQT; ++t) q_issued[t] = -1;
+      bool ok = true;
+      for (long long u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
+        const Unit w = decode_unit(u, p);
+        for (int t = 0; ok && t < kQT; ++t) {
+          ok = ptx::mbar_wait(&q_empty[t], (it & 1) ^ 1, abort_flag, &g_attn_status, lim);
+          if (!ok) break;
+          q_issued[t] = static_cast<int>(it);
+          ptx::mbar_arrive_expect_tx(&q_full[t], C::TILE);
+          for (int h = 0; h < C::NH; ++h)
+            ptx::tma_load_3d(sQ + t * C::TILE + h * kHalfBytes, &tm_q, 64 * h,
+                             w.qb * (kQT * kBM) + t * kBM, w.bh, &q_full[t]);
+        }
+        for (int j = 0; ok && j < w.n; ++j) {
+          for (int which = 0; which < 2; ++which) {
+            const uint32_t st = kv_pos % C::STAGES;
+            const uint32_t ph = (kv_pos / C::STAGES) & 1;
+            ok = ptx::mbar_wait(&kv_empty[st], ph ^ 1, abort_flag, &g_attn_status, lim);
+            if (!ok) break;
+            ptx::mbar_arrive_expect_tx(&kv_full[st], C::TILE);
+            const CUtensorMap* map = which == 0 ? &tm_k : &tm_v;
+            for (int h = 0; h < C::NH; ++h)
+              ptx::tma_load_3d(sKV + st * C::TILE + h * kHalfBytes, map, 64 * h,
+                               w.lo + j * kBN, w.bh, &kv_full[st]);
+            ++kv_pos;
+          }
+        }
+      }
+      if (!ok) {
+        // Error path: let every copy this thread issued land before the CTA's memory goes away.
+        const uint32_t issued = kv_pos < static_cast<uint32_t>(C::STAGES) ? kv_pos : C::STAGES;
+        for (uint32_t i = kv_pos - issued; i < kv_pos; ++i)
+          drain_wait(&kv_full[i % C::STAGES], (i / C::STAGES) & 1, lim);
+        for (int t = 0; t < kQT; ++t)
+          if (q_issued[t] >= 0) drain_wait(&q_full[t], q_issued[t] & 1, lim);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = ptx::idesc_f16(BF16, false, kBM, kBN);
+      constexpr uint32_t kIdescPV = ptx::idesc_f16(BF16, true, kBM, D);
+      const uint32_t sQ_addr = ptx::smem_u32(sQ);
+      const uint32_t sKV_addr = ptx::smem_u32(sKV);
+      const uint32_t s_col[2] = {C::S_COL0, C::S_COL1};
+      const uint32_t o_col[2] = {C::O_COL0, C::O_COL1};
+
+      auto issue_s = [&](int t, uint32_t st) {
+        const uint32_t a0 = sQ_addr + t * C::TILE;
+        const uint32_t b0 = sKV_addr + st * C::TILE;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
+          ptx::mma_ss(tmem + s_col[t], ptx::smem_desc_sw128(a0 + off, 16, 1024),
+                      ptx::smem_desc_sw128(b0 + off, 16, 1024), kIdescS, ks > 0);
+        }
+      };
+      auto issue_pv = [&](int t, uint32_t st, bool acc) {
+        const uint32_t b0 = sKV_addr + st * C::TILE;
+#pragma unroll
+        for (int ks = 0; ks < kBN / 16; ++ks) {
+          ptx::mma_ts(tmem + o_col[t], tmem + s_col[t] + ks * 8,
+                      ptx::smem_desc_sw128(b0 + ks * 2048, kHalfBytes, 1024), kIdescPV,
+                      (acc || ks > 0) ? 1u : 0u);
+        }
+      };
+
+      uint32_t kv_pos = 0, it = 0, pph[2] = {0, 0};
+      bool ok = true;
+      auto wait_kv = [&](uint32_t& st) -> bool {
+        st = kv_pos % C::STAGES;
+        const uint32_t ph = (kv_pos / C::STAGES) & 1;
+        ++kv_pos;
+        return ptx::mbar_wait(&kv_full[st], ph, abort_flag, &g_attn_status, lim);
+      };
+
+      for (long long u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
+        const Unit w = decode_unit(u, p);
+        uint32_t sk, sv;
+        if (!(ok = wait_kv(sk))) break;
+        for (int t = 0; t < kQT; ++t) {
+          if (!(ok = ptx::mbar_wait(&q_full[t], it & 1, abort_flag, &g_attn_status, lim))) break;
+          ptx::tc_fence_after();
+          issue_s(t, sk);
+          ptx::mma_commit(&s_full[t]);
+          if (w.n == 1) ptx::mma_commit(&q_empty[t]);
+        }
+        if (!ok) break;
+        ptx::mma_commit(&kv_empty[sk]);
+
+        for (int j = 1; ok && j <= w.n; ++j) {
+          if (!(ok = wait_kv(sv))) break;
+          for (int t = 0; t < kQT; ++t) {
+            if (!(ok = ptx::mbar_wait(&p_full[t], pph[t], abort_flag, &g_attn_status, lim)))
+              break;
+            pph[t] ^= 1;
+            if (j == 1 && it > 0) {
+              if (!(ok = ptx::mbar_wait(&o_empty[t], (it - 1) & 1, abort_flag, &g_attn_status,
+                                        lim)))
+                break;
+            }
+            ptx::tc_fence_after();
+            issue_pv(t, sv, j > 1);
+            if (t == kQT - 1) ptx::mma_commit(&kv_empty[sv]);
+            if (j == w.n) {
+              ptx::mma_commit(&o_full[t]);
+            } else {
+              if (t == 0 && !(ok = wait_kv(sk))) break;
+              issue_s(t, sk);
+              ptx::mma_commit(&s_full[t]);
+              if (j == w.n - 1) ptx::mma_commit(&q_empty[t]);
+              if (t == kQT - 1) ptx::mma_commit(&kv_empty[sk]);
+            }
+          }
+        }
+      }
+      // All MMAs this thread issued complete before TMEM is released.
+      ptx::mma_commit(mma_drain);
+      drain_wait(mma_drain, 0, lim);
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------------ softmax warpgroups
+    const int t = warp >> 2;                    // query tile of this warpgroup
+    const int wq = warp & 3;                    // TMEM lane quarter
+    const int row = wq * 32 + lane;             // row within the tile
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t s_addr = tmem + lane_base + (t == 0 ? C::S_COL0 : C::S_COL1);
+    const uint32_t o_addr = tmem + lane_base + (t == 0 ? C::O_COL0 : C::O_COL1);
+    const float sl2 = p.scale_log2;
+    uint32_t sph = 0, oph = 0, it = 0;
+    bool ok = true;
+
+    for (long long u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
+      const Unit w = decode_unit(u, p);
+      float m = -INFINITY;   // running max of scaled logits, log2 units
+      float l = 0.f;         // running denominator relative to m
+      for (int j = 0; j < w.n; ++j) {
+        ok = __all_sync(0xffffffffu,
+                        ptx::mbar_wait(&s_full[t], sph, abort_flag, &g_attn_status, lim));
+        if (!ok) break;
+        sph ^= 1;
+        ptx::tc_fence_after();
+
+        float s[kBN];
+#pragma unroll
+        for (int i = 0; i < kBN / 32; ++i) {
+          uint32_t r[32];
+          ptx::tmem_ld32(s_addr + 32 * i, r);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) s[32 * i + c] = __uint_as_float(r[c]);
+        }
+        if (j == w.n - 1 && w.last_valid < kBN) {
+#pragma unroll
+          for (int c = 0; c < kBN; ++c)
+            if (c >= w.last_valid) s[c] = -INFINITY;
+        }
+        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+        for (int c = 4; c < kBN; c += 4) {
+          mx0 = fmaxf(mx0, s[c]);
+          mx1 = fmaxf(mx1, s[c + 1]);
+          mx2 = fmaxf(mx2, s[c + 2]);
+          mx3 = fmaxf(mx3, s[c + 3]);
+        }
+        const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
+        const bool need = m_new > m + kRescaleThreshold;
+        const float alpha = need ? ptx::ex2(m - m_new) : 1.f;   // 0 on the first tile
+        if (need) m = m_new;
+        const float neg_m = -m;
+        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float p0 = ptx::ex2(fmaf(s[64 * h + 2 * c], sl2, neg_m));
+            const float p1 = ptx::ex2(fmaf(s[64 * h + 2 * c + 1], sl2, neg_m));
+            const float p2 = ptx::ex2(fmaf(s[64 * h + 2 * c + 2], sl2, neg_m));
+            const float p3 = ptx::ex2(fmaf(s[64 * h + 2 * c + 3], sl2, neg_m));
+            l0 += p0;
+            l1 += p1;
+            l2 += p2;
+            l3 += p3;
+            pk[c] = ptx::pack2<BF16>(p0, p1);
+            pk[c + 1] = ptx::pack2<BF16>(p2, p3);
+          }
+          ptx::tmem_st32(s_addr + 32 * h, pk);
+        }
+        l = l * alpha + ((l0 + l1) + (l2 + l3));
+        // Rescale O (the P*V of earlier steps, whose MMAs completed before S_j was signalled)
+        // when the max moved in any row of this warp.  P*V of this step is only issued after
+        // the arrive below, so O is not in use.
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+          for (int i = 0; i < D / 32; ++i) {
+            uint32_t r[32];
+            ptx::tmem_ld32(o_addr + 32 * i, r);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
+            ptx::tmem_st32(o_addr + 32 * i, r);
+          }
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&p_full[t]);
+      }
+      if (!ok) break;
+
+      // ---------------------------------------------------------------- epilogue
+      ok = __all_sync(0xffffffffu,
+                      ptx::mbar_wait(&o_full[t], oph, abort_flag, &g_attn_status, lim));
+      if (!ok) break;
+      oph ^= 1;
+      ptx::tc_fence_after();
+      const int q_row = w.qb * (kQT * kBM) + t * kBM + row;
+      const bool valid = q_row < p.Sq;
+      const float inv_l = 1.f / l;
+      const long long prow = static_cast<long long>(w.c) * p.BH + w.bh;
+      uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
+                       (prow * p.Sq + (valid ? q_row : 0)) * static_cast<long long>(D);
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) {
+        uint32_t r[32];
+        ptx::tmem_ld32(o_addr + 32 * i, r);
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          pk[c] = ptx::pack2<BF16>(__uint_as_float(r[2 * c]) * inv_l,
+                                   __uint_as_float(r[2 * c + 1]) * inv_l);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * i);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+      if (valid && p.lse != nullptr)
+        p.lse[prow * p.Sq + q_row] = (m + __log2f(l)) * 0.69314718055994530942f;
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&o_empty[t]);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Watchdog self-test: one thread waits on a barrier nobody arrives on.
+__global__ void watchdog_selftest_kernel(unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    (void)ptx::mbar_wait(&bar, 0, &abort_flag, &g_attn_status, limit_ns);
+  }
+}
+
+// --------------------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 3-D map over a [BH][S][D] 16-bit tensor, box = 64 elements x 128 rows x 1, 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* base, bool bf16, int D, int S, int BH) {
+  auto enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                           static_cast<cuuint64_t>(S) * static_cast<cuuint64_t>(D) * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                   3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D, bool BF16>
+cudaError_t launch_typed(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                         const Params& p, int grid, cudaStream_t stream) {
+  auto kern = attn_fwd_kernel<D, BF16>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Cfg<D>::SMEM);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  kern<<<grid, kThreads, Cfg<D>::SMEM, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+attn_status launch_attention(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int P, int B, int H, int Sq, int Skv, int D, bool bf16, float scale,
+                             cudaStream_t stream, unsigned long long limit_ns, int max_ctas) {
+  const int BH = B * H;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, bf16, D, Sq, BH) || !make_map(&mk, k, bf16, D, Skv, BH) ||
+      !make_map(&mv, v, bf16, D, Skv, BH))
+    return ATTN_ERR_CUDA;
+  Params p;
+  p.Sq = Sq;
+  p.Skv = Skv;
+  p.P = P;
+  p.BH = BH;
+  p.n_qb = (Sq + kQT * kBM - 1) / (kQT * kBM);
+  p.num_units = static_cast<long long>(BH) * P * p.n_qb;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.o = o;
+  p.lse = lse;
+  p.limit_ns = limit_ns;
+  int sms = device_sm_count();
+  if (sms <= 0) return ATTN_ERR_CUDA;
+  if (max_ctas > 0 && max_ctas < sms) sms = max_ctas;
+  const int grid = static_cast<int>(p.num_units < sms ? p.num_units : sms);
+  cudaError_t e;
+  if (D == 128)
+    e = bf16 ? launch_typed<128, true>(mq, mk, mv, p, grid, stream)
+             : launch_typed<128, false>(mq, mk, mv, p, grid, stream);
+  else
+    e = bf16 ? launch_typed<64, true>(mq, mk, mv, p, grid, stream)
+             : launch_typed<64, false>(mq, mk, mv, p, grid, stream);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status launch_watchdog_selftest(unsigned long long limit_ns, cudaStream_t stream) {
+  watchdog_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status read_and_clear_device_status(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  int h = 0;
+  if (cudaMemcpyFromSymbol(&h, g_attn_status, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (h != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_attn_status, &zero, sizeof(int)) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+  }
+  return static_cast<attn_status>(h);
+}
+
+}  // namespace cpattn

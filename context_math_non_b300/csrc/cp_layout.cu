@@ -1,0 +1,107 @@
+// DeepSpeed Ulysses re-partition as an on-device layout permutation (HBM-bound copy kernel).
+//
+// "Scaling AI Inference Across Multiple GPUs Using NVIDIA TensorRT with Multi-Device Inference
+// Support", subsection "DeepSpeed Ulysses" and Figure 4: an all-to-all before attention turns
+// sequence sharding into head sharding, and a second one after attention turns it back.  With all
+// P ranks' shards in one device buffer the all-to-all is a pure index permutation:
+//   seq-sharded  X[p][b][s][h][d]  (rank p holds tokens p*S/P + s, all H heads)
+//   head-sharded Y[g][b][j][t][d]  (rank g holds heads g*H/P + j, all S tokens)
+//   Y[g][b][j][p*S/P + s][d] = X[p][b][s][g*H/P + j][d].
+//
+// Threads walk the head-sharded index space linearly in 16-byte vectors; the matching
+// seq-sharded vector is a run of D*elem_bytes contiguous bytes, so both sides are accessed in
+// whole 16-byte vectors and in runs of at least one (token, head) row.  seq2head reads the
+// seq-sharded side and writes the head-sharded side linearly; head2seq does the reverse.
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "cpattn_internal.h"
+
+namespace cpattn {
+namespace {
+
+constexpr int kLayoutThreads = 256;
+constexpr int kUnroll = 4;
+
+template <typename Idx, bool kSeq2Head>
+__global__ void __launch_bounds__(kLayoutThreads)
+    layout_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, Idx total, int B, int Hl,
+                  int S, int Sl, int H, int vpr) {
+  const Idx step = static_cast<Idx>(gridDim.x) * kLayoutThreads;
+  for (Idx base = static_cast<Idx>(blockIdx.x) * kLayoutThreads * kUnroll + threadIdx.x;
+       base < total; base += step * kUnroll) {
+    uint4 v[kUnroll];
+    Idx dst[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const Idx i = base + static_cast<Idx>(u) * kLayoutThreads;
+      if (i < total) {
+        // head-sharded coordinates of vector i: [g][b][j][t][x]
+        Idx r = i / vpr;
+        const Idx x = i - r * vpr;
+        const Idx t = r % S;
+        r /= S;
+        const Idx j = r % Hl;
+        r /= Hl;
+        const Idx b = r % B;
+        const Idx g = r / B;
+        const Idx p = t / Sl;
+        const Idx s = t - p * Sl;
+        const Idx seq = ((((p * B + b) * Sl + s) * H) + g * Hl + j) * vpr + x;
+        if constexpr (kSeq2Head) {
+          v[u] = __ldcs(in + seq);
+          dst[u] = i;
+        } else {
+          v[u] = __ldcs(in + i);
+          dst[u] = seq;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const Idx i = base + static_cast<Idx>(u) * kLayoutThreads;
+      if (i < total) __stcs(out + dst[u], v[u]);
+    }
+  }
+}
+
+template <typename Idx>
+cudaError_t launch_layout_typed(const void* in, void* out, long long total, int B, int Hl, int S,
+                                int Sl, int H, int vpr, bool seq2head, cudaStream_t stream) {
+  const int sms = device_sm_count();
+  long long blocks = (total + kLayoutThreads * kUnroll - 1) / (kLayoutThreads * kUnroll);
+  const long long cap = static_cast<long long>(sms > 0 ? sms : 148) * 16;
+  if (blocks > cap) blocks = cap;
+  if (seq2head)
+    layout_kernel<Idx, true><<<static_cast<int>(blocks), kLayoutThreads, 0, stream>>>(
+        static_cast<const uint4*>(in), static_cast<uint4*>(out), static_cast<Idx>(total), B, Hl,
+        S, Sl, H, vpr);
+  else
+    layout_kernel<Idx, false><<<static_cast<int>(blocks), kLayoutThreads, 0, stream>>>(
+        static_cast<const uint4*>(in), static_cast<uint4*>(out), static_cast<Idx>(total), B, Hl,
+        S, Sl, H, vpr);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+attn_status launch_layout(const void* in, void* out, int P, int B, int S, int H, int D,
+                          int elem_bytes, bool seq2head, cudaStream_t stream) {
+  const int vpr = D * elem_bytes / 16;
+  const int Hl = H / P;
+  const int Sl = S / P;
+  const long long total = static_cast<long long>(P) * B * Hl * S * vpr;
+  cudaError_t e;
+  // 32-bit index arithmetic when every index (all bounded by total) and the loop counter, which
+  // can step past total by one grid stride, stay far below 2^32.
+  if (total < (1ll << 31))
+    e = launch_layout_typed<uint32_t>(in, out, total, B, Hl, S, Sl, H, vpr, seq2head, stream);
+  else
+    e = launch_layout_typed<unsigned long long>(in, out, total, B, Hl, S, Sl, H, vpr, seq2head,
+                                                stream);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace cpattn

@@ -1,0 +1,31 @@
+// Internal launchers shared between the C ABI (cpattn_capi.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "../../include/cpattn.h"
+
+namespace cpattn {
+
+// Default bound on any single wait inside the attention kernel: 2 seconds.
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
+
+int device_sm_count();
+
+// Attention over P KV chunks (P = 1: plain attention).  Arguments already validated.
+// max_ctas > 0 caps the persistent grid (testing only); 0 = one CTA per SM.
+attn_status launch_attention(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int P, int B, int H, int Sq, int Skv, int D, bool bf16, float scale,
+                             cudaStream_t stream, unsigned long long limit_ns, int max_ctas);
+
+attn_status launch_lse_merge(const void* o_parts, const float* lse_parts, int P, long long rows,
+                             int D, bool bf16, void* o, float* lse, cudaStream_t stream);
+
+attn_status launch_layout(const void* in, void* out, int P, int B, int S, int H, int D,
+                          int elem_bytes, bool seq2head, cudaStream_t stream);
+
+attn_status launch_watchdog_selftest(unsigned long long limit_ns, cudaStream_t stream);
+
+attn_status read_and_clear_device_status(cudaStream_t stream);
+
+}  // namespace cpattn

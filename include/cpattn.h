@@ -1,0 +1,157 @@
+/*
+ * cpattn.h -- C ABI of the context-parallel attention primitives for B300 (sm_103a).
+ *
+ * The operations are those of context-parallel inference for diffusion transformers as described
+ * on "Scaling AI Inference Across Multiple GPUs Using NVIDIA TensorRT with Multi-Device Inference
+ * Support", section "Parallelism strategies for distributed inference" (subsections "Context
+ * parallelism", "Ring Attention", "DeepSpeed Ulysses").  One GPU stands in for P ranks: a ring
+ * step becomes one KV chunk, and the Ulysses all-to-all becomes an on-device re-layout.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The library allocates no device
+ *    memory.  Inputs are never written.  Outputs must not overlap inputs.
+ *  - Tensors are dense and row-major in the order given in brackets (last index contiguous).
+ *  - Every tensor pointer must be 16-byte aligned (ATTN_ERR_MISALIGNED otherwise).
+ *  - Calls are asynchronous on `stream` (NULL = the legacy default stream).  They return after
+ *    the launch.  Argument errors are detected on the host before anything is launched, and then
+ *    nothing is written.  A failed launch returns ATTN_ERR_CUDA.
+ *  - Zero-sized batch / head / query / sequence extents are accepted and launch nothing.
+ *  - The calls are thread-safe and may run concurrently on different streams.  The only
+ *    device-side state is one status word written by the attention kernels' watchdog (see
+ *    attn_device_status).
+ *  - 16-bit types are IEEE fp16 or bfloat16; LSE values are fp32 natural logarithms.
+ */
+#ifndef CPATTN_H
+#define CPATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CPATTN_API __attribute__((visibility("default")))
+#else
+#define CPATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream, declared without the CUDA headers. */
+typedef struct CUstream_st* attn_stream_t;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,  /* null pointer, bad extent, P out of range, overlapping buffers  */
+  ATTN_ERR_UNSUPPORTED = 2,  /* valid request the kernels do not implement (e.g. D not 64/128) */
+  ATTN_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned                                */
+  ATTN_ERR_CUDA = 4,         /* a CUDA runtime / driver call failed                             */
+  ATTN_ERR_TIMEOUT = 5       /* a kernel's bounded wait expired (reported by attn_device_status) */
+} attn_status;
+
+typedef enum { ATTN_BF16 = 0, ATTN_FP16 = 1 } attn_dtype;
+
+/*
+ * attn_fwd -- non-causal multi-head attention forward.
+ *   Defines: page section "Context parallelism" (bidirectional attention of a diffusion
+ *   transformer over the whole sequence): O = softmax(Q K^T * scale) V.
+ *   q   [B][H][Sq][D]   dtype `dt`
+ *   k,v [B][H][Skv][D]  dtype `dt`
+ *   o   [B][H][Sq][D]   dtype `dt`, written (fp32 accumulation, rounded to nearest even)
+ *   lse [B][H][Sq] fp32, written if non-NULL: ln sum_j exp(scale * q.k_j)
+ *   D must be 64 or 128 (ATTN_ERR_UNSUPPORTED otherwise); Skv >= 1.
+ *   scale <= 0 selects 1/sqrt(D).
+ */
+CPATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int H, int Sq, int Skv, int D, attn_dtype dt, float scale,
+                     attn_stream_t stream);
+
+/*
+ * attn_fwd_chunked -- per-KV-chunk partial outputs (one ring step per chunk).
+ *   Defines: page subsection "Ring Attention" and Figure 3: each rank holds a slice of K and V,
+ *   and the attention output is built up slice by slice with an online softmax.
+ *   KV rows are split into P contiguous chunks; chunk c covers rows
+ *   [floor(c*Skv/P), floor((c+1)*Skv/P)).  For each chunk the kernel writes the attention of Q
+ *   over that chunk only, normalised over the chunk, and its LSE:
+ *   o_parts   [P][B][H][Sq][D]  dtype `dt`
+ *   lse_parts [P][B][H][Sq]     fp32 (required)
+ *   attn_lse_merge of these partials reproduces attn_fwd.  1 <= P <= Skv; other arguments as
+ *   for attn_fwd.
+ */
+CPATTN_API attn_status attn_fwd_chunked(const void* q, const void* k, const void* v, int P,
+                             void* o_parts, float* lse_parts,
+                             int B, int H, int Sq, int Skv, int D, attn_dtype dt, float scale,
+                             attn_stream_t stream);
+
+/*
+ * attn_lse_merge -- combine P partial attention outputs by their log-sum-exp.
+ *   Defines: page subsection "Ring Attention" (the output is updated as each KV block streams
+ *   past).  Per row, with M = max_c LSE_c and w_c = exp(LSE_c - M):
+ *     O = sum_c w_c O_c / sum_c w_c,  LSE = M + ln sum_c w_c.
+ *   A row whose partials all have LSE = -inf merges to O = 0, LSE = -inf.
+ *   o_parts   [P][B][H][Sq][D] dtype `dt`;  lse_parts [P][B][H][Sq] fp32
+ *   o         [B][H][Sq][D]    dtype `dt`;  lse [B][H][Sq] fp32, written if non-NULL
+ *   P >= 1; D >= 1 with D * 2 bytes a multiple of 16.
+ */
+CPATTN_API attn_status attn_lse_merge(const void* o_parts, const float* lse_parts, int P,
+                           int B, int H, int Sq, int D, attn_dtype dt,
+                           void* o, float* lse, attn_stream_t stream);
+
+/*
+ * cp_layout_seq2head -- the first DeepSpeed Ulysses all-to-all, as one on-device re-layout.
+ *   Defines: page subsection "DeepSpeed Ulysses" and Figure 4: sequence sharding becomes head
+ *   sharding, every rank then holding the full sequence for a disjoint subset of heads.
+ *   in  [P][B][S/P][H][D]   rank p holds tokens p*S/P .. (p+1)*S/P-1, all heads
+ *   out [P][B][H/P][S][D]   rank g holds all tokens (global order), heads g*H/P .. (g+1)*H/P-1
+ *   out[g][b][j][p*S/P + s][d] = in[p][b][s][g*H/P + j][d]  (bit copy of elem_bytes each)
+ *   Requires P >= 1, S % P == 0, H % P == 0, (D * elem_bytes) % 16 == 0, no overlap.
+ */
+CPATTN_API attn_status cp_layout_seq2head(const void* in, void* out, int P, int B, int S, int H, int D,
+                               int elem_bytes, attn_stream_t stream);
+
+/*
+ * cp_layout_head2seq -- the second Ulysses all-to-all: exact inverse of cp_layout_seq2head.
+ *   Defines: page subsection "DeepSpeed Ulysses" (results gathered across heads and
+ *   re-partitioned along the sequence).
+ *   in  [P][B][H/P][S][D] -> out [P][B][S/P][H][D]; same requirements.
+ */
+CPATTN_API attn_status cp_layout_head2seq(const void* in, void* out, int P, int B, int S, int H, int D,
+                               int elem_bytes, attn_stream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+CPATTN_API const char* attn_status_string(attn_status status);
+
+/*
+ * attn_device_status -- synchronise `stream`, then return and clear the device status word.
+ *   The attention kernels bound every internal wait; a wait that expires records
+ *   ATTN_ERR_TIMEOUT there and the kernel returns early instead of hanging (its outputs are then
+ *   undefined).  Returns ATTN_OK if nothing was recorded, ATTN_ERR_CUDA if the synchronisation
+ *   itself failed.
+ */
+CPATTN_API attn_status attn_device_status(attn_stream_t stream);
+
+/*
+ * attn_watchdog_selftest -- launch one block that waits, with the attention kernels' bounded
+ *   wait, on a barrier that nothing ever signals, giving up after `limit_ns` nanoseconds
+ *   (clamped to [1e3, 1e10]).  The expected outcome is that attn_device_status then reports
+ *   ATTN_ERR_TIMEOUT.  Exists so the failure path can be tested without faulting a GPU.
+ */
+CPATTN_API attn_status attn_watchdog_selftest(uint64_t limit_ns, attn_stream_t stream);
+
+/*
+ * attn_set_max_ctas -- cap the persistent attention grid at `n` CTAs (n <= 0 restores the
+ *   default of one CTA per SM).  Process-wide; affects launches made after the call.  Used to
+ *   exercise the many-units-per-CTA path on small problems and to study load balance.  Returns
+ *   the previous cap.
+ */
+CPATTN_API int attn_set_max_ctas(int n);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+CPATTN_API int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPATTN_H */

@@ -1,0 +1,144 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function the header declares,
+and rejects invalid arguments on the host (before any CUDA call) with the documented status.
+
+Pointers passed here are fake addresses; every case below is rejected (or is an empty problem)
+before the library touches the device, which is exactly what these tests pin down.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from context_math_non_b300 import cpattn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "cpattn.h")
+
+A = 0x7f0000000000          # fake, 16-byte aligned "device" addresses, far apart
+B_ = 0x7f0010000000
+C = 0x7f0020000000
+O = 0x7f0030000000
+L = 0x7f0040000000
+BIG = 1 << 20
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^CPATTN_API\s+(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*"
+                                 r"([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def L_():
+    if not os.path.exists(cpattn.LIB_PATH):
+        from context_math_non_b300.build import build
+        build()
+    return cpattn.lib()
+
+
+def test_header_declares_the_boundary():
+    fns = declared_functions()
+    for name in ("attn_fwd", "attn_fwd_chunked", "attn_lse_merge", "cp_layout_seq2head",
+                 "cp_layout_head2seq", "attn_status_string", "attn_device_status",
+                 "attn_watchdog_selftest"):
+        assert name in fns, name
+
+
+def test_library_exports_every_declared_symbol(L_):
+    for name in declared_functions():
+        assert hasattr(L_, name), f"libcpattn.so does not export {name}"
+
+
+def test_library_exports_nothing_undeclared(L_):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", cpattn.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    ours = {s for s in exported if s.startswith(("attn_", "cp_layout_"))}
+    assert ours == set(declared_functions())
+
+
+def test_status_strings(L_):
+    assert cpattn.attn_status_string(0) == "ATTN_OK"
+    assert cpattn.attn_status_string(5) == "ATTN_ERR_TIMEOUT"
+    assert cpattn.attn_status_string(99) == "ATTN_ERR_UNKNOWN"
+    assert cpattn.attn_version() >= 100
+
+
+def test_max_ctas_setter(L_):
+    prev = cpattn.attn_set_max_ctas(7)
+    assert cpattn.attn_set_max_ctas(0) == 7
+    assert cpattn.attn_set_max_ctas(prev) == 0
+
+
+def fwd(L_, q=A, k=B_, v=C, o=O, lse=L, B=1, H=2, Sq=256, Skv=256, D=64, dt=0, scale=0.0):
+    return L_.attn_fwd(q, k, v, o, lse, B, H, Sq, Skv, D, dt, scale, None)
+
+
+def chunked(L_, P=4, q=A, k=B_, v=C, o=O, lse=L, B=1, H=2, Sq=256, Skv=256, D=64, dt=0):
+    return L_.attn_fwd_chunked(q, k, v, P, o, lse, B, H, Sq, Skv, D, dt, 0.0, None)
+
+
+def test_attention_argument_errors(L_):
+    E, U, M = cpattn.ATTN_ERR_INVALID_ARG, cpattn.ATTN_ERR_UNSUPPORTED, cpattn.ATTN_ERR_MISALIGNED
+    assert fwd(L_, q=None) == E
+    assert fwd(L_, o=None) == E
+    assert fwd(L_, Skv=0) == E
+    assert fwd(L_, B=-1) == E
+    assert fwd(L_, dt=7) == E
+    assert fwd(L_, D=96) == U
+    assert fwd(L_, D=256) == U
+    assert fwd(L_, q=A + 8) == M
+    assert fwd(L_, lse=L + 4) == M
+    assert fwd(L_, o=A) == E                        # output aliases q
+    assert fwd(L_, lse=B_ + 64) == E                # lse inside k
+    assert chunked(L_, P=0) == E
+    assert chunked(L_, P=257) == E                  # more chunks than KV rows
+    assert chunked(L_, lse=None) == E               # partial LSEs are required
+    assert chunked(L_, o=O, lse=O + 1024) == E      # the two outputs overlap
+
+
+def test_attention_empty_problems_launch_nothing(L_):
+    # zero batch / heads / queries: OK without any device work (fake pointers never touched)
+    assert fwd(L_, B=0) == cpattn.ATTN_OK
+    assert fwd(L_, H=0) == cpattn.ATTN_OK
+    assert fwd(L_, Sq=0) == cpattn.ATTN_OK
+    assert chunked(L_, Sq=0) == cpattn.ATTN_OK
+
+
+def test_merge_argument_errors(L_):
+    E, M = cpattn.ATTN_ERR_INVALID_ARG, cpattn.ATTN_ERR_MISALIGNED
+    f = L_.attn_lse_merge
+    assert f(None, L, 4, 1, 2, 8, 64, 0, O, None, None) == E
+    assert f(A, L, 0, 1, 2, 8, 64, 0, O, None, None) == E
+    assert f(A, L, 4, 1, 2, 8, 60, 0, O, None, None) == E          # D*2 not a multiple of 16
+    assert f(A, L, 4, 1, 2, 8, 64, 3, O, None, None) == E
+    assert f(A + 2, L, 4, 1, 2, 8, 64, 0, O, None, None) == M
+    assert f(A, L, 4, 1, 2, 8, 64, 0, A + 64, None, None) == E     # o inside o_parts
+    assert f(A, L, 4, 1, 2, 8, 64, 0, O, L, None) == E             # lse aliases lse_parts
+    assert f(A, L, 4, 0, 2, 8, 64, 0, O, None, None) == cpattn.ATTN_OK
+
+
+@pytest.mark.parametrize("fn", ["cp_layout_seq2head", "cp_layout_head2seq"])
+def test_layout_argument_errors(L_, fn):
+    E, M = cpattn.ATTN_ERR_INVALID_ARG, cpattn.ATTN_ERR_MISALIGNED
+    f = getattr(L_, fn)
+    assert f(None, O, 8, 2, 64, 32, 64, 2, None) == E
+    assert f(A, O, 0, 2, 64, 32, 64, 2, None) == E
+    assert f(A, O, 8, 2, 60, 32, 64, 2, None) == E     # S % P
+    assert f(A, O, 8, 2, 64, 30, 64, 2, None) == E     # H % P
+    assert f(A, O, 8, 2, 64, 32, 3, 2, None) == E      # D*elem_bytes % 16
+    assert f(A, O, 8, 2, 64, 32, 64, 0, None) == E
+    assert f(A + 4, O, 8, 2, 64, 32, 64, 2, None) == M
+    assert f(A, A + 256, 8, 2, 64, 32, 64, 2, None) == E   # in-place / overlapping
+    assert f(A, O, 8, 0, 64, 32, 64, 2, None) == cpattn.ATTN_OK
+    assert f(A, O, 8, 2, 0, 32, 64, 2, None) == cpattn.ATTN_OK
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(cpattn, "_lib", None)
+    monkeypatch.setattr(cpattn, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(cpattn.CpAttnLibraryError):
+        cpattn.lib()

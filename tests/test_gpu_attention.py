@@ -1,0 +1,153 @@
+"""GPU parity of the tcgen05 attention kernel (attn_fwd / attn_fwd_chunked) against the float64
+oracle, through the C ABI.  Small shapes are compared element by element over every output;
+the full-size workloads are compared on sampled query rows (all heads, all D columns, and the
+LSE), which the oracle computes row by row."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from context_math_non_b300 import cpattn
+from context_math_non_b300.inputs import WORKLOADS, draw_qkv
+from parity import assert_attention_close, oracle_rows, sample_rows, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def rand_qkv(B, H, Sq, Skv, D, dtype, seed, q_scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    q = (torch.randn(B, H, Sq, D, generator=g) * q_scale).to(dtype)
+    k = torch.randn(B, H, Skv, D, generator=g).to(dtype)
+    v = torch.randn(B, H, Skv, D, generator=g).to(dtype)
+    return q, k, v
+
+
+def run_full_and_chunked(q, k, v, P, what):
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o, lse = cpattn.attn_fwd(qd, kd, vd)
+    op, lp = cpattn.attn_fwd_chunked(qd, kd, vd, P)
+    om, lm = cpattn.attn_lse_merge(op, lp)
+    assert cpattn.attn_device_status() == cpattn.ATTN_OK
+    o_ref, lse_ref = oracle.attention(q, k, v)
+    op_ref, lp_ref = oracle.attention_chunked(q, k, v, P)
+    assert_attention_close(o, lse, o_ref, lse_ref, f"{what} attn_fwd")
+    assert_attention_close(op, lp, op_ref, lp_ref, f"{what} chunked P={P}")
+    assert_attention_close(om, lm, o_ref, lse_ref, f"{what} chunked P={P} + merge")
+    return o, lse
+
+
+def test_tiny_workload():
+    """B=1 H=2 S=256 D=64, bf16-rounded N(0,1) draws; P=4 chunks merged and P=1."""
+    (q, k, v) = draw_qkv(WORKLOADS["tiny"])
+    run_full_and_chunked(q, k, v, 4, "tiny")
+
+
+SMALL_CASES = [
+    # B, H, Sq, Skv, D, dtype, P
+    (1, 3, 1000, 1000, 128, torch.bfloat16, 3),   # ragged tiles and chunk bounds (333/333/334)
+    (1, 3, 1000, 1000, 128, torch.bfloat16, 8),   # chunks of 125 rows (< one tile)
+    (2, 2, 300, 777, 64, torch.float16, 5),       # Sq != Skv, D = 64, fp16
+    (1, 2, 129, 5, 64, torch.bfloat16, 5),        # P = Skv: one KV row per chunk
+    (1, 1, 1, 1, 128, torch.bfloat16, 1),         # single query, single key
+    (1, 2, 640, 640, 128, torch.float16, 2),      # exact tiles, fp16, D = 128
+    (3, 1, 200, 300, 64, torch.bfloat16, 2),      # batch > 1
+    (1, 4, 576, 4608, 128, torch.bfloat16, 8),    # AllGather-KV shape: local queries, full KV
+]
+
+
+@pytest.mark.parametrize("B,H,Sq,Skv,D,dtype,P", SMALL_CASES)
+def test_small_shapes(B, H, Sq, Skv, D, dtype, P):
+    q, k, v = rand_qkv(B, H, Sq, Skv, D, dtype, seed=Sq * 31 + Skv + P)
+    run_full_and_chunked(q, k, v, P, f"B{B} H{H} Sq{Sq} Skv{Skv} D{D} {dtype}")
+
+
+def test_large_logits_no_overflow():
+    """Logits of magnitude ~100 (fp32 exp overflows without the running-max shift)."""
+    q, k, v = rand_qkv(1, 2, 384, 700, 128, torch.bfloat16, seed=5, q_scale=12.0)
+    run_full_and_chunked(q, k, v, 3, "large logits")
+
+
+def test_many_units_per_cta():
+    """A grid capped at 2 CTAs walks 36 units each: exercises every barrier phase wrap."""
+    q, k, v = rand_qkv(1, 3, 1000, 1000, 128, torch.bfloat16, seed=11)
+    prev = cpattn.attn_set_max_ctas(2)
+    try:
+        run_full_and_chunked(q, k, v, 3, "2 CTAs")
+    finally:
+        cpattn.attn_set_max_ctas(prev)
+
+
+def test_deterministic():
+    q, k, v = (t.cuda() for t in rand_qkv(1, 4, 700, 900, 128, torch.bfloat16, seed=3))
+    a = cpattn.attn_fwd_chunked(q, k, v, 3)
+    b = cpattn.attn_fwd_chunked(q, k, v, 3)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_outputs_stay_in_bounds():
+    """Canary regions around o_parts / lse_parts are untouched (ragged Sq = 1000)."""
+    B, H, Sq, Skv, D, P = 1, 2, 1000, 600, 128, 3
+    q, k, v = (t.cuda() for t in rand_qkv(B, H, Sq, Skv, D, torch.bfloat16, seed=9))
+    n_o, n_l, pad = P * B * H * Sq * D, P * B * H * Sq, 4096
+    obuf = torch.full((n_o + 2 * pad,), 7.0, dtype=torch.bfloat16, device="cuda")
+    lbuf = torch.full((n_l + 2 * pad,), -3.0, dtype=torch.float32, device="cuda")
+    op = obuf[pad:pad + n_o].view(P, B, H, Sq, D)
+    lp = lbuf[pad:pad + n_l].view(P, B, H, Sq)
+    cpattn.attn_fwd_chunked(q, k, v, P, op, lp)
+    torch.cuda.synchronize()
+    assert (obuf[:pad] == 7.0).all() and (obuf[pad + n_o:] == 7.0).all()
+    assert (lbuf[:pad] == -3.0).all() and (lbuf[pad + n_l:] == -3.0).all()
+    assert torch.isfinite(op.float()).all() and torch.isfinite(lp).all()
+
+
+# ----------------------------------------------------------------------------- full sizes
+
+@pytest.fixture(scope="module")
+def image_inputs():
+    return draw_qkv(WORKLOADS["image"])
+
+
+@pytest.mark.parametrize("P", [1, 2, 4, 8])
+def test_image_workload_sampled(image_inputs, P):
+    """B=1 H=24 S=4608 D=128 bf16, KV in P chunks; sampled query rows of every head."""
+    q, k, v = image_inputs
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    rows = sample_rows(4608, 24, seed=100 + P)
+    if P == 1:
+        o, lse = cpattn.attn_fwd(qd, kd, vd)
+        o_ref, lse_ref = oracle_rows(q, k, v, rows)
+        assert_attention_close(o[:, :, rows].cpu(), lse[:, :, rows].cpu(), o_ref, lse_ref,
+                               "image P=1")
+        return
+    op, lp = cpattn.attn_fwd_chunked(qd, kd, vd, P)
+    om, lm = cpattn.attn_lse_merge(op, lp)
+    assert cpattn.attn_device_status() == cpattn.ATTN_OK
+    op_ref, lp_ref = oracle_rows(q, k, v, rows, P)
+    assert_attention_close(op[:, :, :, rows].cpu(), lp[:, :, :, rows].cpu(), op_ref, lp_ref,
+                           f"image chunked P={P}")
+    o_ref, lse_ref = oracle.lse_merge(op_ref, lp_ref)
+    assert_attention_close(om[:, :, rows].cpu(), lm[:, :, rows].cpu(), o_ref, lse_ref,
+                           f"image P={P} merged")
+
+
+@pytest.mark.parametrize("name", ["video", "stress"])
+def test_long_sequence_workloads_sampled(name):
+    """video: B=1 H=16 S=44160 D=128, P=8 (chunks of 5520 = 43*128 + 16 rows);
+    stress: B=1 H=16 S=32768, Q x4 and 1 % of K rows x8, P=8.  Sampled rows of every head."""
+    w = WORKLOADS[name]
+    q, k, v = draw_qkv(w)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    op, lp = cpattn.attn_fwd_chunked(qd, kd, vd, 8)
+    om, lm = cpattn.attn_lse_merge(op, lp)
+    assert cpattn.attn_device_status() == cpattn.ATTN_OK
+    rows = sample_rows(w.S, 40, seed=w.seed)
+    op_ref, lp_ref = oracle_rows(q, k, v, rows, 8)
+    assert_attention_close(op[:, :, :, rows].cpu(), lp[:, :, :, rows].cpu(), op_ref, lp_ref,
+                           f"{name} chunked")
+    o_ref, lse_ref = oracle_rows(q, k, v, rows)
+    assert_attention_close(om[:, :, rows].cpu(), lm[:, :, rows].cpu(), o_ref, lse_ref,
+                           f"{name} merged vs unchunked oracle")
+    # the merge itself, fed the GPU's own partials
+    om_ref, lm_ref = oracle.lse_merge(to_np(op[:, :, :, rows]), to_np(lp[:, :, :, rows]))
+    assert_attention_close(om[:, :, rows].cpu(), lm[:, :, rows].cpu(), om_ref, lm_ref,
+                           f"{name} merge of GPU partials")
