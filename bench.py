@@ -394,6 +394,36 @@ def run_reference(args):
     }
 
 
+def run_profile_case(args):
+    """One kernel only, for an ncu capture: W + K launches on a reduced case that still exceeds
+    L2 -- attn: the video shape with --heads heads (default 2: Q/K/V 22.6 MB each, partials
+    181 MB), P=8; merge: the same partials; layout: the Ulysses shape (134 MB each side)."""
+    from context_math_non_b300 import cpattn
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = WORKLOAD
+    H = args.heads or 2
+    if args.profile in ("attn", "merge"):
+        q, k, v = (t.to(dev) for t in draw_qkv(w, H=H))
+        op, lp = cpattn.attn_fwd_chunked(q, k, v, P_CHUNKS)
+        for _ in range(args.warmup + args.steps):
+            if args.profile == "attn":
+                cpattn.attn_fwd_chunked(q, k, v, P_CHUNKS, op, lp)
+            else:
+                cpattn.attn_lse_merge(op, lp)
+    else:
+        wu = WORKLOADS["ulysses"]
+        x = draw_qkv(wu)[0].to(dev)
+        y = cpattn.cp_layout_seq2head(x)
+        for _ in range(args.warmup + args.steps):
+            cpattn.cp_layout_seq2head(x, y)
+    torch.cuda.synchronize(dev)
+    st = cpattn.attn_device_status()
+    if st != cpattn.ATTN_OK:
+        raise RuntimeError(cpattn.attn_status_string(st))
+    print(f"profile case {args.profile} done", flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -404,10 +434,16 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=24)
+    ap.add_argument("--profile", choices=["attn", "merge", "layout"], default=None,
+                    help="run one kernel on the reduced profiling case (for ncu) and exit")
+    ap.add_argument("--heads", type=int, default=None)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local_rank = _dist()
+    if args.profile:
+        run_profile_case(args)
+        return
 
     if args.impl == "reference":
         if rank == 0:

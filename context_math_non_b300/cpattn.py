@@ -19,7 +19,9 @@ __all__ = ["CpAttnError", "CpAttnLibraryError", "lib", "attn_fwd", "attn_fwd_chu
            "LIB_PATH", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
            "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT"]
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcpattn.so")
+# CPATTN_LIBRARY may point at another build of the same library (e.g. a debug build).
+LIB_PATH = os.environ.get("CPATTN_LIBRARY") or os.path.join(
+    os.path.dirname(os.path.abspath(__file__)), "libcpattn.so")
 
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED = 0, 1, 2
 ATTN_ERR_MISALIGNED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = 3, 4, 5

@@ -16,7 +16,8 @@
 //   warps 4-7  softmax for query tile 1
 //   warp  8    TMA producer: Q tiles once per unit, then K_j / V_j through a ring of stages
 //   warp  9    TMEM allocation and the single MMA-issuing thread
-//   warps 10-11 idle (they complete the third warpgroup)
+//   warps 10-11 idle (they complete the third warpgroup, which releases registers to the
+//              softmax warpgroups with setmaxnreg)
 // Tensor memory (512 columns): S0 | S1 | O0 | O1.  P (16-bit) is written over the first half of
 // its S columns and read from TMEM by the P*V MMA.  The MMA order per KV step j
 //   O0 += P0 V_{j-1};  S0 = Q0 K_j^T;  O1 += P1 V_{j-1};  S1 = Q1 K_j^T
@@ -49,6 +50,17 @@ constexpr int kBN = 128;          // KV rows per tile
 constexpr int kQT = 2;            // query tiles per CTA
 constexpr int kHalfBytes = 128 * 128;  // [128 rows][64 x 16-bit] swizzled box = 16 KB
 constexpr int kThreads = 384;
+// Register split: the kernel is compiled for kLaunchRegs per thread (the 384-thread launch
+// bound); the producer warpgroup gives registers back (setmaxnreg.dec) and the two softmax
+// warpgroups take them (setmaxnreg.inc).  The increase must be covered by what is released,
+// or setmaxnreg.inc would wait forever; the host refuses to launch a build whose register
+// count differs from kLaunchRegs.
+constexpr int kLaunchRegs = 168;
+constexpr int kSoftmaxRegs = 192;
+constexpr int kProducerRegs = 112;
+static_assert(2 * 128 * (kSoftmaxRegs - kLaunchRegs) <= 128 * (kLaunchRegs - kProducerRegs),
+              "setmaxnreg increase exceeds the registers released by the producer warpgroup");
+static_assert(kLaunchRegs * kThreads <= 65536, "register file");
 
 constexpr int kLoaderWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -68,10 +80,11 @@ struct Cfg {
 
 struct Params {
   int Sq, Skv, P, BH, n_qb;
-  long long num_units;
+  int num_units;     // BH * P * n_qb (< 2^31, checked on the host)
+  int kv_q, kv_r;    // Skv = kv_q * P + kv_r
   float scale_log2;
-  void* o;      // [P][BH][Sq][D]
-  float* lse;   // [P][BH][Sq] or null
+  void* o;           // [P][BH][Sq][D]
+  float* lse;        // [P][BH][Sq] or null
   unsigned long long limit_ns;
 };
 
@@ -79,16 +92,23 @@ struct Unit {
   int qb, c, bh, lo, n, last_valid;
 };
 
-__device__ __forceinline__ Unit decode_unit(long long u, const Params& p) {
+// Chunk c covers KV rows [floor(c*Skv/P), floor((c+1)*Skv/P)); with Skv = q*P + r,
+// floor(c*Skv/P) = c*q + floor(c*r/P), and c*r < P^2 <= 2^32 fits 32-bit unsigned arithmetic.
+__device__ __forceinline__ int chunk_start(int c, const Params& p) {
+  return c * p.kv_q + static_cast<int>((static_cast<uint32_t>(c) * static_cast<uint32_t>(p.kv_r)) /
+                                       static_cast<uint32_t>(p.P));
+}
+
+__device__ __forceinline__ Unit decode_unit(int u, const Params& p) {
   Unit w;
-  w.qb = static_cast<int>(u % p.n_qb);
-  long long r = u / p.n_qb;
-  w.c = static_cast<int>(r % p.P);
-  w.bh = static_cast<int>(r / p.P);
-  const long long lo = static_cast<long long>(w.c) * p.Skv / p.P;
-  const long long hi = static_cast<long long>(w.c + 1) * p.Skv / p.P;
-  const int len = static_cast<int>(hi - lo);
-  w.lo = static_cast<int>(lo);
+  const uint32_t uu = static_cast<uint32_t>(u);
+  const uint32_t r = uu / static_cast<uint32_t>(p.n_qb);
+  w.qb = static_cast<int>(uu - r * static_cast<uint32_t>(p.n_qb));
+  const uint32_t bh = r / static_cast<uint32_t>(p.P);
+  w.c = static_cast<int>(r - bh * static_cast<uint32_t>(p.P));
+  w.bh = static_cast<int>(bh);
+  w.lo = chunk_start(w.c, p);
+  const int len = chunk_start(w.c + 1, p) - w.lo;
   w.n = (len + kBN - 1) / kBN;
   w.last_valid = len - (w.n - 1) * kBN;
   return w;
@@ -100,6 +120,100 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
   const uint64_t t0 = ptx::globaltimer_ns();
   while (!ptx::mbar_try_wait(bar, parity)) {
     if (ptx::globaltimer_ns() - t0 > limit_ns) return;
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[D]) {
+  if constexpr (D == 128) {
+    ptx::tmem_ld128(taddr, r);
+  } else {
+    ptx::tmem_ld64(taddr, r);
+  }
+}
+
+// One KV tile of the online softmax for this thread's row: read the 128 logits from TMEM,
+// update the running max m (only when it grows by more than the threshold; `need` reports a
+// move and `alpha` = 2^(m_old - m_new), or 1), write P = 2^(s*scale*log2e - m) as 16-bit pairs
+// over the first 64 columns of the same TMEM region, and return the row sum of P.  kMasked
+// treats columns >= valid as -inf (last tile of a KV chunk).
+template <bool BF16, bool kMasked>
+__device__ __forceinline__ float softmax_tile(uint32_t s_addr, float sl2, int valid, float& m,
+                                              bool& need, float& alpha) {
+  uint32_t sr[kBN];
+  ptx::tmem_ld128(s_addr, sr);
+  if constexpr (kMasked) {
+#pragma unroll
+    for (int c = 0; c < kBN; ++c)
+      if (c >= valid) sr[c] = __float_as_uint(-INFINITY);
+  }
+#define SV(c) __uint_as_float(sr[c])
+  float mx0 = SV(0), mx1 = SV(1), mx2 = SV(2), mx3 = SV(3);
+#pragma unroll
+  for (int c = 4; c + 8 <= kBN; c += 8) {
+    mx0 = ptx::max3(mx0, SV(c), SV(c + 1));
+    mx1 = ptx::max3(mx1, SV(c + 2), SV(c + 3));
+    mx2 = ptx::max3(mx2, SV(c + 4), SV(c + 5));
+    mx3 = ptx::max3(mx3, SV(c + 6), SV(c + 7));
+  }
+  mx0 = ptx::max3(mx0, SV(kBN - 4), SV(kBN - 3));
+  mx1 = ptx::max3(mx1, SV(kBN - 2), SV(kBN - 1));
+  const float m_new = fmaxf(m, ptx::max3(mx0, mx1, fmaxf(mx2, mx3)) * sl2);
+  need = m_new > m + kRescaleThreshold;
+  alpha = need ? ptx::ex2(m - m_new) : 1.f;   // 0 on the first tile (m = -inf)
+  if (need) m = m_new;
+  // p = 2^(s*scale*log2(e) - m), two elements per packed fp32x2 FMA / ADD.
+  const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
+  const uint64_t negm2 = ptx::f2_pack(-m, -m);
+  uint64_t lacc[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) lacc[a] = ptx::f2_pack(0.f, 0.f);
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int e = 32 * h + 2 * c;
+      const uint64_t x = ptx::f2_fma(ptx::f2_pack(SV(e), SV(e + 1)), sl2x2, negm2);
+      float x0, x1;
+      ptx::f2_unpack(x, x0, x1);
+      const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+      lacc[c & 3] = ptx::f2_add(lacc[c & 3], ptx::f2_pack(p0, p1));
+      pk[c] = ptx::pack2<BF16>(p0, p1);
+    }
+    ptx::tmem_st16(s_addr + 16 * h, pk);
+  }
+#undef SV
+  float la, lb;
+  ptx::f2_unpack(ptx::f2_add(ptx::f2_add(lacc[0], lacc[1]), ptx::f2_add(lacc[2], lacc[3])), la,
+                 lb);
+  return la + lb;
+}
+
+// O row *= alpha for this thread's TMEM lane, 64 columns per load round trip.
+template <int D>
+__device__ __forceinline__ void rescale_o(uint32_t o_addr, float alpha) {
+  const uint64_t a2 = ptx::f2_pack(alpha, alpha);
+#pragma unroll
+  for (int half = 0; half < D / 64; ++half) {
+    uint32_t r[64];
+    ptx::tmem_ld64(o_addr + 64 * half, r);
+#pragma unroll
+    for (int c = 0; c < 64; c += 2) {
+      float x0, x1;
+      ptx::f2_unpack(
+          ptx::f2_mul(ptx::f2_pack(__uint_as_float(r[c]), __uint_as_float(r[c + 1])), a2), x0,
+          x1);
+      r[c] = __float_as_uint(x0);
+      r[c + 1] = __float_as_uint(x1);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t q[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) q[c] = r[16 * i + c];
+      ptx::tmem_st16(o_addr + 64 * half + 16 * i, q);
+    }
   }
 }
 
@@ -162,6 +276,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  if (warp >= 8) {
+    // Producer warpgroup: hand registers to the softmax warpgroups.
+    ptx::regs_dec<kProducerRegs>();
   if (warp == kLoaderWarp) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -169,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int q_issued[kQT];
       for (int t = 0; t < kQT; ++t) q_issued[t] = -1;
       bool ok = true;
-      for (long long u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
+      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
         const Unit w = decode_unit(u, p);
         for (int t = 0; ok && t < kQT; ++t) {
           ok = ptx::mbar_wait(&q_empty[t], (it & 1) ^ 1, abort_flag, &g_attn_status, lim);
@@ -243,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return ptx::mbar_wait(&kv_full[st], ph, abort_flag, &g_attn_status, lim);
       };
 
-      for (long long u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
+      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
         const Unit w = decode_unit(u, p);
         uint32_t sk, sv;
         if (!(ok = wait_kv(sk))) break;
@@ -287,8 +404,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mma_commit(mma_drain);
       drain_wait(mma_drain, 0, lim);
     }
-  } else if (warp < 8) {
+  }
+  } else {
     // ------------------------------------------------------------------ softmax warpgroups
+    ptx::regs_inc<kSoftmaxRegs>();
     const int t = warp >> 2;                    // query tile of this warpgroup
     const int wq = warp & 3;                    // TMEM lane quarter
     const int row = wq * 32 + lane;             // row within the tile
@@ -299,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t sph = 0, oph = 0, it = 0;
     bool ok = true;
 
-    for (long long u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
+    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
       const Unit w = decode_unit(u, p);
       float m = -INFINITY;   // running max of scaled logits, log2 units
       float l = 0.f;         // running denominator relative to m
@@ -310,65 +429,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         sph ^= 1;
         ptx::tc_fence_after();
 
-        float s[kBN];
-#pragma unroll
-        for (int i = 0; i < kBN / 32; ++i) {
-          uint32_t r[32];
-          ptx::tmem_ld32(s_addr + 32 * i, r);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) s[32 * i + c] = __uint_as_float(r[c]);
-        }
-        if (j == w.n - 1 && w.last_valid < kBN) {
-#pragma unroll
-          for (int c = 0; c < kBN; ++c)
-            if (c >= w.last_valid) s[c] = -INFINITY;
-        }
-        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
-#pragma unroll
-        for (int c = 4; c < kBN; c += 4) {
-          mx0 = fmaxf(mx0, s[c]);
-          mx1 = fmaxf(mx1, s[c + 1]);
-          mx2 = fmaxf(mx2, s[c + 2]);
-          mx3 = fmaxf(mx3, s[c + 3]);
-        }
-        const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
-        const bool need = m_new > m + kRescaleThreshold;
-        const float alpha = need ? ptx::ex2(m - m_new) : 1.f;   // 0 on the first tile
-        if (need) m = m_new;
-        const float neg_m = -m;
-        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const float p0 = ptx::ex2(fmaf(s[64 * h + 2 * c], sl2, neg_m));
-            const float p1 = ptx::ex2(fmaf(s[64 * h + 2 * c + 1], sl2, neg_m));
-            const float p2 = ptx::ex2(fmaf(s[64 * h + 2 * c + 2], sl2, neg_m));
-            const float p3 = ptx::ex2(fmaf(s[64 * h + 2 * c + 3], sl2, neg_m));
-            l0 += p0;
-            l1 += p1;
-            l2 += p2;
-            l3 += p3;
-            pk[c] = ptx::pack2<BF16>(p0, p1);
-            pk[c + 1] = ptx::pack2<BF16>(p2, p3);
-          }
-          ptx::tmem_st32(s_addr + 32 * h, pk);
-        }
-        l = l * alpha + ((l0 + l1) + (l2 + l3));
+        bool need;
+        float alpha;
+        const float l_tile =
+            (j == w.n - 1 && w.last_valid < kBN)
+                ? softmax_tile<BF16, true>(s_addr, sl2, w.last_valid, m, need, alpha)
+                : softmax_tile<BF16, false>(s_addr, sl2, kBN, m, need, alpha);
+        l = l * alpha + l_tile;
         // Rescale O (the P*V of earlier steps, whose MMAs completed before S_j was signalled)
         // when the max moved in any row of this warp.  P*V of this step is only issued after
         // the arrive below, so O is not in use.
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
-#pragma unroll
-          for (int i = 0; i < D / 32; ++i) {
-            uint32_t r[32];
-            ptx::tmem_ld32(o_addr + 32 * i, r);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
-            ptx::tmem_st32(o_addr + 32 * i, r);
-          }
-        }
+        if (j > 0 && __any_sync(0xffffffffu, need)) rescale_o<D>(o_addr, alpha);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         __syncwarp();
@@ -389,19 +460,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
                        (prow * p.Sq + (valid ? q_row : 0)) * static_cast<long long>(D);
 #pragma unroll
-      for (int i = 0; i < D / 32; ++i) {
-        uint32_t r[32];
-        ptx::tmem_ld32(o_addr + 32 * i, r);
-        uint32_t pk[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          pk[c] = ptx::pack2<BF16>(__uint_as_float(r[2 * c]) * inv_l,
-                                   __uint_as_float(r[2 * c + 1]) * inv_l);
+      for (int half = 0; half < D / 64; ++half) {
+        uint32_t orr[64];
+        ptx::tmem_ld64(o_addr + 64 * half, orr);
         if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * i);
+          uint4* dst = reinterpret_cast<uint4*>(orow + 64 * half);
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          for (int v = 0; v < 8; ++v) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              pk[c] = ptx::pack2<BF16>(__uint_as_float(orr[8 * v + 2 * c]) * inv_l,
+                                       __uint_as_float(orr[8 * v + 2 * c + 1]) * inv_l);
+            dst[v] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
         }
       }
       if (valid && p.lse != nullptr)
@@ -473,11 +545,16 @@ cudaError_t launch_typed(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
   auto kern = attn_fwd_kernel<D, BF16>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
+  static int regs = -1;
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     Cfg<D>::SMEM);
+    cudaFuncAttributes fa;
+    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, kern);
+    if (attr_err == cudaSuccess) regs = fa.numRegs;
   });
   if (attr_err != cudaSuccess) return attr_err;
+  if (regs != kLaunchRegs) return cudaErrorInvalidKernelImage;   // see the register split
   kern<<<grid, kThreads, Cfg<D>::SMEM, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
@@ -506,7 +583,11 @@ attn_status launch_attention(const void* q, const void* k, const void* v, void* 
   p.P = P;
   p.BH = BH;
   p.n_qb = (Sq + kQT * kBM - 1) / (kQT * kBM);
-  p.num_units = static_cast<long long>(BH) * P * p.n_qb;
+  const long long units = static_cast<long long>(BH) * P * p.n_qb;
+  if (units >= (1ll << 31) || P > 65536) return ATTN_ERR_UNSUPPORTED;
+  p.num_units = static_cast<int>(units);
+  p.kv_q = Skv / P;
+  p.kv_r = Skv % P;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.o = o;
   p.lse = lse;
@@ -514,7 +595,7 @@ attn_status launch_attention(const void* q, const void* k, const void* v, void* 
   int sms = device_sm_count();
   if (sms <= 0) return ATTN_ERR_CUDA;
   if (max_ctas > 0 && max_ctas < sms) sms = max_ctas;
-  const int grid = static_cast<int>(p.num_units < sms ? p.num_units : sms);
+  const int grid = p.num_units < sms ? p.num_units : sms;
   cudaError_t e;
   if (D == 128)
     e = bf16 ? launch_typed<128, true>(mq, mk, mv, p, grid, stream)

@@ -2,7 +2,11 @@
 
 Tolerances for attention (max |dO| <= 1e-2, mean |dO| <= 1e-3, max |dLSE| <= 1e-3, absolute,
 against the float64 oracle on the same 16-bit inputs) are the ones the build targets for bf16
-attention with fp32 accumulation; the layout kernels must be bit-exact.  The merge in isolation
+attention with fp32 accumulation.  The max-|dO| bound is applied on top of the unavoidable
+rounding of the stored output: an element may also differ by half an ulp of the output type at
+the reference value (2^-8 relative for bf16, 2^-11 for fp16), since even the exact result
+rounded to bf16 misses by up to 0.0156 once |O| >= 4.  For N(0,1) workloads |O| << 1 and this
+term is below 1e-3.  The layout kernels must be bit-exact.  The merge in isolation
 is held to what its own arithmetic allows: output rounding to the 16-bit type (half an ulp,
 2^-9 relative for bf16, 2^-12 for fp16) plus fp32 accumulation error.
 """
@@ -20,11 +24,26 @@ def to_np(t: torch.Tensor) -> np.ndarray:
     return t.detach().to("cpu", torch.float64).numpy()
 
 
-def assert_attention_close(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
-    o = to_np(o_gpu) if isinstance(o_gpu, torch.Tensor) else o_gpu
+def half_ulp(x: np.ndarray, dtype) -> np.ndarray:
+    """Half the spacing of the 16-bit output type at |x| (normal range)."""
+    mant = 7 if dtype == torch.bfloat16 else 10
+    ax = np.maximum(np.abs(x), 2.0 ** -14)
+    return np.exp2(np.floor(np.log2(ax)) - mant - 1)
+
+
+def assert_attention_close(o_gpu, lse_gpu, o_ref, lse_ref, what="", dtype=None):
+    if isinstance(o_gpu, torch.Tensor):
+        dtype = o_gpu.dtype
+        o = to_np(o_gpu)
+    else:
+        o = o_gpu
+    dtype = torch.bfloat16 if dtype is None else dtype
     assert np.isfinite(o).all(), f"{what}: non-finite output"
     err = np.abs(o - o_ref)
-    assert err.max() <= TOL_MAX, f"{what}: max |dO| = {err.max():.3e}"
+    excess = err - half_ulp(o_ref, dtype)
+    i = np.unravel_index(np.argmax(excess), err.shape)
+    assert excess.max() <= TOL_MAX, (f"{what}: |dO| = {err[i]:.3e} at |O| = {abs(o_ref[i]):.3f} "
+                                     f"exceeds 1e-2 + half ulp; max |dO| = {err.max():.3e}")
     assert err.mean() <= TOL_MEAN, f"{what}: mean |dO| = {err.mean():.3e}"
     if lse_gpu is not None:
         lse = to_np(lse_gpu) if isinstance(lse_gpu, torch.Tensor) else lse_gpu
