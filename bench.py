@@ -9,6 +9,8 @@ oracle timed on a bounded sample.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
                     [--no-cpu-baseline] [--no-e2e]
+    python bench.py --profile attn|merge|layout    # one kernel, reduced case, for ncu
+    python bench.py --probe                         # tensor-core calibration probes
 
 Prints one JSON line (rank 0).  With torchrun each rank runs an independent replica of the same
 workload on its own GPU (the path needs no exchange on one box); ``value`` is the sum over ranks
@@ -56,6 +58,22 @@ def _dist():
     return 0, 1, 0
 
 
+def reduce_max(value: float, device) -> float:
+    """Max of `value` over all ranks (the slowest rank's time); identity on one process."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return value
+    if torch.distributed.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tflops(world: int, flops_per_step: float, steps: int, ms: float) -> float:
+    """Whole-job throughput: every rank does flops_per_step per step (weak scaling)."""
+    return world * flops_per_step * steps / (ms * 1e-3) / 1e12
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -98,6 +116,7 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
+        self.skip = 0
 
     def __enter__(self):
         try:
@@ -107,6 +126,10 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 3.0:   # sampler running before timing
+                time.sleep(0.02)
+            self.skip = len(self.lines)
         except OSError:
             self.proc = None
         return self
@@ -128,7 +151,7 @@ class ClockSampler:
         sm, mx = [], None
         reasons = set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in self.lines[self.skip:]:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) != 6:
                 continue
@@ -200,12 +223,9 @@ def run_native(args, rank, world, local_rank):
     if st != cpattn.ATTN_OK:
         raise RuntimeError(f"device status after timing: {cpattn.attn_status_string(st)}")
 
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max(total_ms, dev)
     ms_per_step = total_ms / args.steps
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = aggregate_tflops(world, flops, args.steps, total_ms)
 
     peaks = _peaks()
     attn_avg = sum(attn_ms) / len(attn_ms)
@@ -314,14 +334,10 @@ def _e2e_leg(cpattn, q, k, v, dev, stream, args, flops, world):
         step()
     b.record(stream)
     torch.cuda.synchronize(dev)
-    ms = a.elapsed_time(b)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(a.elapsed_time(b), dev)
     h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
     d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
-    return {"value": round(world * flops * steps / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
+    return {"value": round(aggregate_tflops(world, flops, steps, ms), 2), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": round(ms / steps, 3)}
 
@@ -351,10 +367,16 @@ def cpu_baseline(q, k, v, budget_s: float = 15.0):
     """The float64 oracle, as it stands, timed on this host on a bounded sample of the same
     workload: R query rows of every head through chunked attention (P=8) and the merge."""
     w = WORKLOAD
-    t0 = time.perf_counter()
-    _oracle_sample(q, k, v, 32, 1)                  # calibration (also warms BLAS)
-    t_cal = time.perf_counter() - t0
-    per_row = t_cal / 32
+    _oracle_sample(q, k, v, 16, 1)                  # warm BLAS and the allocator
+    rows = 32
+    while True:                                     # calibrate on one head
+        t0 = time.perf_counter()
+        _oracle_sample(q, k, v, rows, 1)
+        t_cal = time.perf_counter() - t0
+        if t_cal >= 0.05 * budget_s or rows >= w.S:
+            break
+        rows = min(w.S, rows * 2)
+    per_row = t_cal / rows
     rows = int(max(16, min(w.S, budget_s / per_row / w.H)))
     t0 = time.perf_counter()
     _oracle_sample(q, k, v, rows, w.H)
@@ -424,6 +446,46 @@ def run_profile_case(args):
     print(f"profile case {args.profile} done", flush=True)
 
 
+def run_mma_probe():
+    """Tensor-core calibration (attn_probe_mma): achievable tcgen05 rates of the MMA forms the
+    attention kernel uses, its per-step sequence with and without neighbours, and the latency
+    of one GEMM -> consumer -> GEMM hand-off.  Prints one JSON line."""
+    from context_math_non_b300 import cpattn
+    torch.cuda.set_device(0)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def rate(n, mode, iters):
+        cpattn.attn_probe_mma(n, mode, max(32, iters // 20))
+        torch.cuda.synchronize()
+        a.record()
+        cpattn.attn_probe_mma(n, mode, iters)
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    out = {"unit": "TFLOP/s", "sms": sms}
+    names = {0: "SS", 1: "TS"}
+    for n in (64, 128, 256):
+        for mode in (0, 1):
+            ms = rate(n, mode, 20000)
+            out[f"M128_N{n}_{names[mode]}"] = round(sms * 20000 * 2 * 128 * n * 16 / ms / 1e9, 1)
+    labels = {2: "attention_step_sequence", 3: "step_sequence_with_fence",
+              5: "step_sequence_with_tmem_streaming_neighbours",
+              6: "step_sequence_with_dependent_fma_neighbours",
+              7: "step_sequence_with_independent_fma_neighbours"}
+    for mode, label in labels.items():
+        ms = rate(128, mode, 64000)
+        out[label] = round(sms * 64000 * 2 * 128 * 128 * 16 / ms / 1e9, 1)
+    ms = rate(128, 4, 32000)
+    out["handoff_round_trip_ns"] = round(ms * 1e6 / 4000, 1)
+    out["gemm_128x128x128_ns_at_peak"] = round(2 * 128 ** 3 / (2.26e15 / sms) * 1e9, 1)
+    st = cpattn.attn_device_status()
+    if st != cpattn.ATTN_OK:
+        raise RuntimeError(cpattn.attn_status_string(st))
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -437,12 +499,17 @@ def main():
     ap.add_argument("--profile", choices=["attn", "merge", "layout"], default=None,
                     help="run one kernel on the reduced profiling case (for ncu) and exit")
     ap.add_argument("--heads", type=int, default=None)
+    ap.add_argument("--probe", action="store_true",
+                    help="run the tensor-core calibration probes and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local_rank = _dist()
     if args.profile:
         run_profile_case(args)
+        return
+    if args.probe:
+        run_mma_probe()
         return
 
     if args.impl == "reference":

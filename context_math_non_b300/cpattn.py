@@ -15,7 +15,7 @@ import torch
 
 __all__ = ["CpAttnError", "CpAttnLibraryError", "lib", "attn_fwd", "attn_fwd_chunked",
            "attn_lse_merge", "cp_layout_seq2head", "cp_layout_head2seq", "attn_device_status",
-           "attn_watchdog_selftest", "attn_set_max_ctas", "attn_status_string", "attn_version",
+           "attn_watchdog_selftest", "attn_set_max_ctas", "attn_probe_mma", "attn_status_string", "attn_version",
            "LIB_PATH", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
            "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT"]
 
@@ -64,10 +64,11 @@ def lib() -> ctypes.CDLL:
     L.attn_device_status.argtypes = [vp]
     L.attn_watchdog_selftest.argtypes = [ctypes.c_uint64, vp]
     L.attn_set_max_ctas.argtypes = [i]
+    L.attn_probe_mma.argtypes = [i, i, i, vp]
     L.attn_version.argtypes = []
     for name in ("attn_fwd", "attn_fwd_chunked", "attn_lse_merge", "cp_layout_seq2head",
                  "cp_layout_head2seq", "attn_device_status", "attn_watchdog_selftest",
-                 "attn_set_max_ctas", "attn_version"):
+                 "attn_set_max_ctas", "attn_version", "attn_probe_mma"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -175,6 +176,12 @@ def cp_layout_head2seq(y: torch.Tensor, out: Optional[torch.Tensor] = None, stre
     _check("cp_layout_head2seq", lib().cp_layout_head2seq(
         _dev(y, "in"), _dev(out, "out"), P, B, S, Hl * P, D, y.element_size(), _stream(stream)))
     return out
+
+
+def attn_probe_mma(n: int, mode: int, iters: int, stream=None):
+    """Launch the tensor-core ceiling probe (time it with CUDA events around the call)."""
+    _check("attn_probe_mma", lib().attn_probe_mma(int(n), int(mode), int(iters),
+                                                   _stream(stream)))
 
 
 def attn_device_status(stream=None) -> int:

@@ -8,10 +8,9 @@
 //   head-sharded Y[g][b][j][t][d]  (rank g holds heads g*H/P + j, all S tokens)
 //   Y[g][b][j][p*S/P + s][d] = X[p][b][s][g*H/P + j][d].
 //
-// Threads walk the head-sharded index space linearly in 16-byte vectors; the matching
-// seq-sharded vector is a run of D*elem_bytes contiguous bytes, so both sides are accessed in
-// whole 16-byte vectors and in runs of at least one (token, head) row.  seq2head reads the
-// seq-sharded side and writes the head-sharded side linearly; head2seq does the reverse.
+// Threads walk one side's index space linearly in 16-byte vectors; the matching vector on the
+// other side is part of a run of D*elem_bytes contiguous bytes, so both sides are accessed in
+// whole 16-byte vectors and in runs of at least one (token, head) row.
 
 #include <cuda_runtime.h>
 
@@ -24,8 +23,11 @@ namespace {
 
 constexpr int kLayoutThreads = 256;
 constexpr int kUnroll = 4;
+constexpr bool kSeq2HeadWalksHead = true;   // seq2head walks its destination (head-sharded) space
 
-template <typename Idx, bool kSeq2Head>
+// kHeadLinear: threads walk the head-sharded index space linearly (true) or the sequence-sharded
+// one (false); the other side is then accessed in runs of one (token, head) row.
+template <typename Idx, bool kSeq2Head, bool kHeadLinear>
 __global__ void __launch_bounds__(kLayoutThreads)
     layout_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, Idx total, int B, int Hl,
                   int S, int Sl, int H, int vpr) {
@@ -38,24 +40,42 @@ __global__ void __launch_bounds__(kLayoutThreads)
     for (int u = 0; u < kUnroll; ++u) {
       const Idx i = base + static_cast<Idx>(u) * kLayoutThreads;
       if (i < total) {
-        // head-sharded coordinates of vector i: [g][b][j][t][x]
-        Idx r = i / vpr;
-        const Idx x = i - r * vpr;
-        const Idx t = r % S;
-        r /= S;
-        const Idx j = r % Hl;
-        r /= Hl;
-        const Idx b = r % B;
-        const Idx g = r / B;
-        const Idx p = t / Sl;
-        const Idx s = t - p * Sl;
-        const Idx seq = ((((p * B + b) * Sl + s) * H) + g * Hl + j) * vpr + x;
-        if constexpr (kSeq2Head) {
-          v[u] = __ldcs(in + seq);
-          dst[u] = i;
+        Idx head_i, seq_i;
+        if constexpr (kHeadLinear) {
+          // head-sharded coordinates of vector i: [g][b][j][t][x]
+          Idx r = i / vpr;
+          const Idx x = i - r * vpr;
+          const Idx t = r % S;
+          r /= S;
+          const Idx j = r % Hl;
+          r /= Hl;
+          const Idx b = r % B;
+          const Idx g = r / B;
+          const Idx p = t / Sl;
+          const Idx s = t - p * Sl;
+          head_i = i;
+          seq_i = ((((p * B + b) * Sl + s) * H) + g * Hl + j) * vpr + x;
         } else {
-          v[u] = __ldcs(in + i);
-          dst[u] = seq;
+          // sequence-sharded coordinates of vector i: [p][b][s][h][x]
+          Idx r = i / vpr;
+          const Idx x = i - r * vpr;
+          const Idx h = r % H;
+          r /= H;
+          const Idx s = r % Sl;
+          r /= Sl;
+          const Idx b = r % B;
+          const Idx p = r / B;
+          const Idx g = h / Hl;
+          const Idx j = h - g * Hl;
+          seq_i = i;
+          head_i = (((g * B + b) * Hl + j) * S + p * Sl + s) * vpr + x;
+        }
+        if constexpr (kSeq2Head) {
+          v[u] = __ldcs(in + seq_i);
+          dst[u] = head_i;
+        } else {
+          v[u] = __ldcs(in + head_i);
+          dst[u] = seq_i;
         }
       }
     }
@@ -74,12 +94,16 @@ cudaError_t launch_layout_typed(const void* in, void* out, long long total, int 
   long long blocks = (total + kLayoutThreads * kUnroll - 1) / (kLayoutThreads * kUnroll);
   const long long cap = static_cast<long long>(sms > 0 ? sms : 148) * 16;
   if (blocks > cap) blocks = cap;
+  // Both directions write linearly (the destination is walked in order) and gather the source
+  // in runs of one (token, head) row.
   if (seq2head)
-    layout_kernel<Idx, true><<<static_cast<int>(blocks), kLayoutThreads, 0, stream>>>(
+    layout_kernel<Idx, true, kSeq2HeadWalksHead><<<static_cast<int>(blocks), kLayoutThreads, 0,
+                                                   stream>>>(
         static_cast<const uint4*>(in), static_cast<uint4*>(out), static_cast<Idx>(total), B, Hl,
         S, Sl, H, vpr);
   else
-    layout_kernel<Idx, false><<<static_cast<int>(blocks), kLayoutThreads, 0, stream>>>(
+    layout_kernel<Idx, false, !kSeq2HeadWalksHead><<<static_cast<int>(blocks), kLayoutThreads, 0,
+                                                     stream>>>(
         static_cast<const uint4*>(in), static_cast<uint4*>(out), static_cast<Idx>(total), B, Hl,
         S, Sl, H, vpr);
   return cudaGetLastError();

@@ -28,4 +28,6 @@ attn_status launch_watchdog_selftest(unsigned long long limit_ns, cudaStream_t s
 
 attn_status read_and_clear_device_status(cudaStream_t stream);
 
+attn_status launch_mma_probe(int n, int mode, int iters, cudaStream_t stream);
+
 }  // namespace cpattn

@@ -8,9 +8,10 @@
 //   LSE = M + ln sum_c w_c.
 //
 // One thread owns one 16-byte vector (8 elements) of one row and streams that vector of every
-// partial; the P loads of a group are issued back to back so they are in flight together.  The
-// row's LSE values are read by all threads of the row (L1 broadcast).  Inputs are read once and
-// output written once, so loads/stores use the streaming cache hints.
+// partial; the LSE values and O vectors of a group of partials are all issued before any is
+// used, so they are in flight together.  The row's LSE values are read by all threads of the row
+// (L1 broadcast).  Inputs are read once and output written once, so loads/stores use the
+// streaming cache hints.
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -45,9 +46,12 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
   }
 }
 
-// VPR = 16-byte vectors per row (0 = runtime value `vpr`).
+// VPR = 16-byte vectors per row (0 = runtime value `vpr`).  Partials are taken in groups of
+// kGroup: all LSE values and O vectors of a group are loaded before any is used, and groups are
+// combined with a running maximum (acc and W rescaled by exp(M_old - M_new) when it moves), which
+// for P <= kGroup is exactly the one-pass formula.
 template <bool BF16, int VPR>
-__global__ void __launch_bounds__(kMergeThreads)
+__global__ void __launch_bounds__(kMergeThreads, 3)
     lse_merge_kernel(const uint4* __restrict__ o_parts, const float* __restrict__ lse_parts,
                      int P, long long rows, int vpr_rt, uint4* __restrict__ o,
                      float* __restrict__ lse_out) {
@@ -59,46 +63,57 @@ __global__ void __launch_bounds__(kMergeThreads)
        i += static_cast<long long>(gridDim.x) * kMergeThreads) {
     const long long r = i / vpr;
     const int col = static_cast<int>(i - r * vpr);
-    const float* lrow = lse_parts + r;
-    float M = -INFINITY;
-    for (int c = 0; c < P; ++c) M = fmaxf(M, __ldg(lrow + static_cast<long long>(c) * rows));
     float acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
     float W = 0.f;
-    if (M != -INFINITY) {
-      const float Ml2 = M * kLog2e;
-      for (int c0 = 0; c0 < P; c0 += kGroup) {
-        uint4 v[kGroup];
-        float wgt[kGroup];
+    float Ml2 = -INFINITY;   // running max of LSE * log2(e)
+    for (int c0 = 0; c0 < P; c0 += kGroup) {
+      uint4 v[kGroup];
+      float ls[kGroup];
 #pragma unroll
-        for (int g = 0; g < kGroup; ++g) {
-          if (c0 + g < P) {
-            v[g] = __ldcs(o_parts + static_cast<long long>(c0 + g) * part_stride + i);
-            wgt[g] = ptx::ex2(fmaf(__ldg(lrow + static_cast<long long>(c0 + g) * rows), kLog2e,
-                                   -Ml2));
-          }
+      for (int g = 0; g < kGroup; ++g) {
+        if (c0 + g < P) {
+          ls[g] = __ldg(lse_parts + static_cast<long long>(c0 + g) * rows + r) * kLog2e;
+          v[g] = __ldcs(o_parts + static_cast<long long>(c0 + g) * part_stride + i);
+        } else {
+          ls[g] = -INFINITY;
         }
+      }
+      float mg = ls[0];
 #pragma unroll
-        for (int g = 0; g < kGroup; ++g) {
-          if (c0 + g < P) {
-            float f[8];
-            unpack8<BF16>(v[g], f);
-            W += wgt[g];
+      for (int g = 1; g < kGroup; ++g) mg = fmaxf(mg, ls[g]);
+      const float m_new = fmaxf(Ml2, mg);
+      if (m_new == -INFINITY) continue;        // every partial so far is empty
+      if (m_new > Ml2) {
+        const float sc = ptx::ex2(Ml2 - m_new);   // 0 while Ml2 = -inf
+        W *= sc;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = fmaf(wgt[g], f[e], acc[e]);
-          }
+        for (int e = 0; e < 8; ++e) acc[e] *= sc;
+        Ml2 = m_new;
+      }
+#pragma unroll
+      for (int g = 0; g < kGroup; ++g) {
+        if (c0 + g < P) {
+          const float wgt = ptx::ex2(ls[g] - Ml2);
+          float f[8];
+          unpack8<BF16>(v[g], f);
+          W += wgt;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[e] = fmaf(wgt, f[e], acc[e]);
         }
       }
     }
-    const float inv = M != -INFINITY ? 1.f / W : 0.f;
+    const bool empty = Ml2 == -INFINITY;
+    const float inv = empty ? 0.f : 1.f / W;
     uint4 out;
     out.x = ptx::pack2<BF16>(acc[0] * inv, acc[1] * inv);
     out.y = ptx::pack2<BF16>(acc[2] * inv, acc[3] * inv);
     out.z = ptx::pack2<BF16>(acc[4] * inv, acc[5] * inv);
     out.w = ptx::pack2<BF16>(acc[6] * inv, acc[7] * inv);
     __stcs(o + i, out);
-    if (lse_out != nullptr && col == 0) lse_out[r] = M != -INFINITY ? M + logf(W) : -INFINITY;
+    if (lse_out != nullptr && col == 0)
+      lse_out[r] = empty ? -INFINITY : (Ml2 + log2f(W)) * 0.69314718055994530942f;
   }
 }
 
@@ -108,7 +123,7 @@ cudaError_t launch_merge_typed(const void* o_parts, const float* lse_parts, int 
   const long long total = rows * vpr;
   const int sms = device_sm_count();
   long long blocks = (total + kMergeThreads - 1) / kMergeThreads;
-  const long long cap = static_cast<long long>(sms > 0 ? sms : 148) * 8;
+  const long long cap = static_cast<long long>(sms > 0 ? sms : 148) * 3;
   if (blocks > cap) blocks = cap;
   lse_merge_kernel<BF16, VPR><<<static_cast<int>(blocks), kMergeThreads, 0, stream>>>(
       static_cast<const uint4*>(o_parts), lse_parts, P, rows, vpr, static_cast<uint4*>(o), lse);

@@ -1,0 +1,222 @@
+// Tensor-core ceiling probe: tcgen05.mma issued back to back with no data movement.
+//
+// One CTA per SM allocates tensor memory, zeroes a shared-memory operand buffer, and a single
+// thread issues `iters` kind::f16 MMAs (M = 128, N = n, K = 16, fp32 accumulation) -- operands
+// from shared memory (SS) or A from tensor memory (TS), the two forms the attention kernel uses
+// for S = Q K^T and O += P V.  Timing the launch gives the achievable MMA rate of each form,
+// the denominator against which the attention kernel's pipeline is judged.  Mode "step" issues
+// the attention kernel's per-KV-step sequence instead (P0*V, Q0*K^T, P1*V, Q1*K^T with N = 128,
+// alternating accumulators, one commit after each GEMM), counting 4 GEMMs of 8 MMAs per step.
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "cpattn_internal.h"
+#include "ptx_sm103.cuh"
+
+namespace cpattn {
+namespace {
+
+__device__ int g_probe_status = 0;
+constexpr int kProbeSmem = 2 * 128 * 256 * 2 + 1024;   // A and B operand space (bf16)
+
+// kMode: 0 = SS, 1 = TS, 2 = attention step pattern, 3 = same + fence, 4 = ping-pong: one
+// 128x128x128 GEMM, commit, a consumer warp waits for it, reads 32 TMEM columns and arrives on a
+// second barrier, which the MMA thread waits for before the next GEMM (serial round trips);
+// 5 = step pattern while warps 4-7 stream tensor-memory loads (128 columns) and stores (64
+// columns) like the softmax does; 6 = step pattern while warps 4-7 run dependent FMA chains;
+// 7 = the same with eight independent FMA chains per thread (issue-bound background).
+template <int N, int kMode>
+__global__ void __launch_bounds__(256, 1) mma_probe_kernel(int iters) {
+  constexpr bool kTS = kMode == 1;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  __shared__ uint64_t done;
+  __shared__ uint64_t sink;
+  __shared__ uint64_t ping;
+  __shared__ int abort_flag;
+  __shared__ volatile int stop_flag;
+  __shared__ uint32_t tmem_slot;
+  // Operands: random bf16 values in about [-2, 2] (a hash of the index), so the tensor core
+  // does real work; zero operands would understate power draw.
+  for (int i = threadIdx.x; i < 2 * 128 * 256 * 2 / 4; i += blockDim.x) {
+    uint32_t h = static_cast<uint32_t>(i) * 2654435761u;
+    h ^= h >> 15;
+    h *= 2246822519u;
+    h ^= h >> 13;
+    const uint32_t e0 = 0x3F00u | ((h >> 8) & 0x80FFu), e1 = 0x3F00u | ((h >> 24) | ((h << 7) & 0x8000u));
+    reinterpret_cast<uint32_t*>(smem)[i] = (e0 & 0xBFFFu) | ((e1 & 0xBFFFu) << 16);
+  }
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&done, 1);
+    ptx::mbar_init(&sink, 1);
+    ptx::mbar_init(&ping, 1);
+    abort_flag = 0;
+    stop_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (threadIdx.x < 32) {
+    ptx::tmem_alloc(&tmem_slot, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  if constexpr (kMode == 4) {
+    const uint32_t a_addr = ptx::smem_u32(smem);
+    const uint32_t b_addr = a_addr + 128 * 256 * 2;
+    constexpr uint32_t idesc = ptx::idesc_f16(true, false, 128, 128);
+    const int rounds = iters / 8;
+    if (threadIdx.x == 0) {
+      for (int r = 0; r < rounds; ++r) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+          ptx::mma_ss(tmem, ptx::smem_desc_sw128(a_addr + off, 16, 1024),
+                      ptx::smem_desc_sw128(b_addr + off, 16, 1024), idesc, ks > 0);
+        }
+        ptx::mma_commit(&sink);
+        if (!ptx::mbar_wait(&ping, r & 1, &abort_flag, &g_probe_status, 2000000000ull)) break;
+        ptx::tc_fence_after();
+      }
+    } else if (threadIdx.x >= 32 && threadIdx.x < 64) {
+      for (int r = 0; r < rounds; ++r) {
+        const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(&sink, r & 1, &abort_flag,
+                                                               &g_probe_status, 2000000000ull));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        uint32_t v[32];
+        ptx::tmem_ld32(tmem + (32u << 16), v);
+        ptx::tc_fence_before();
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(&ping);
+        if (v[0] == 0xFFFFFFFFu && v[31] == 0x12345678u) abort_flag = 1;   // keep the load
+      }
+    }
+  } else if (threadIdx.x == 0) {
+    const uint32_t a_addr = ptx::smem_u32(smem);
+    const uint32_t b_addr = a_addr + 128 * 256 * 2;
+    constexpr uint32_t idesc = ptx::idesc_f16(true, false, 128, N);
+    if constexpr (kMode == 2 || kMode == 3 || kMode >= 5) {
+      constexpr uint32_t idesc_pv = ptx::idesc_f16(true, true, 128, N);
+      for (int i = 0; i < iters / 32; ++i) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if constexpr (kMode == 3) ptx::tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            ptx::mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + ks * 8,
+                        ptx::smem_desc_sw128(b_addr + ks * 2048, 16384, 1024), idesc_pv, 1u);
+          ptx::mma_commit(&sink);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            ptx::mma_ss(tmem + 128 * t, ptx::smem_desc_sw128(a_addr + off, 16, 1024),
+                        ptx::smem_desc_sw128(b_addr + off, 16, 1024), idesc, ks > 0);
+          }
+          ptx::mma_commit(&sink);
+        }
+        ptx::mma_commit(&sink);
+      }
+    }
+    for (int i = 0; i < (kMode >= 2 ? 0 : iters); ++i) {
+      const uint32_t off = (i & 3) * 32;
+      const uint64_t bd = ptx::smem_desc_sw128(b_addr + off, 16, 1024);
+      if constexpr (kTS) {
+        ptx::mma_ts(tmem + 256, tmem + (i & 3) * 8, bd, idesc, 1u);
+      } else {
+        ptx::mma_ss(tmem, ptx::smem_desc_sw128(a_addr + off, 16, 1024), bd, idesc, 1u);
+      }
+    }
+    ptx::mma_commit(&done);
+    volatile int dummy_abort = 0;
+    int dummy_status = 0;
+    (void)ptx::mbar_wait(&done, 0, &dummy_abort, &dummy_status, 2000000000ull);
+    stop_flag = 1;
+  } else if (kMode >= 5 && threadIdx.x >= 128) {
+    // background load on warps 4-7 (TMEM lane quarter = warp % 4) until the MMAs are done
+    const uint32_t lane_base = static_cast<uint32_t>(((threadIdx.x >> 5) & 3) * 32) << 16;
+    float acc = threadIdx.x;
+    uint32_t sink_v = 0;
+    for (int guard = 0; guard < (1 << 24) && !stop_flag; ++guard) {
+      if constexpr (kMode == 5) {
+        uint32_t r[128];
+        ptx::tmem_ld128(tmem + lane_base + 128, r);
+        uint32_t q[16];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) q[c] = r[32 * h + c] ^ r[32 * h + 16 + c];
+          ptx::tmem_st16(tmem + lane_base + 128 + 16 * h, q);
+        }
+        ptx::tmem_st_wait();
+        sink_v += r[7];
+      } else if constexpr (kMode == 6) {
+#pragma unroll 16
+        for (int c = 0; c < 256; ++c) acc = fmaf(acc, 1.0001f, 0.5f);
+      } else {
+        float a8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a8[i] = acc + i;
+#pragma unroll 4
+        for (int c = 0; c < 64; ++c) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) a8[i] = fmaf(a8[i], 1.0001f, 0.5f);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc += a8[i];
+      }
+    }
+    if (acc == 1.2345f && sink_v == 77u) abort_flag = 1;
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int N, int kMode>
+cudaError_t launch_probe(int iters, int grid, cudaStream_t stream) {
+  auto k = mma_probe_kernel<N, kMode>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kProbeSmem);
+  if (e != cudaSuccess) return e;
+  k<<<grid, kMode >= 5 ? 256 : 128, kProbeSmem, stream>>>(iters);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+attn_status launch_mma_probe(int n, int mode, int iters, cudaStream_t stream) {
+  const int grid = device_sm_count();
+  if (grid <= 0) return ATTN_ERR_CUDA;
+  cudaError_t e;
+  if (mode == 2)
+    e = launch_probe<128, 2>(iters, grid, stream);
+  else if (mode == 3)
+    e = launch_probe<128, 3>(iters, grid, stream);
+  else if (mode == 4)
+    e = launch_probe<128, 4>(iters, grid, stream);
+  else if (mode == 5)
+    e = launch_probe<128, 5>(iters, grid, stream);
+  else if (mode == 6)
+    e = launch_probe<128, 6>(iters, grid, stream);
+  else if (mode == 7)
+    e = launch_probe<128, 7>(iters, grid, stream);
+  else if (n == 64)
+    e = mode ? launch_probe<64, 1>(iters, grid, stream) : launch_probe<64, 0>(iters, grid, stream);
+  else if (n == 128)
+    e = mode ? launch_probe<128, 1>(iters, grid, stream)
+             : launch_probe<128, 0>(iters, grid, stream);
+  else
+    e = mode ? launch_probe<256, 1>(iters, grid, stream)
+             : launch_probe<256, 0>(iters, grid, stream);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace cpattn

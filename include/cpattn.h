@@ -147,6 +147,22 @@ CPATTN_API attn_status attn_watchdog_selftest(uint64_t limit_ns, attn_stream_t s
  */
 CPATTN_API int attn_set_max_ctas(int n);
 
+/*
+ * attn_probe_mma -- tensor-core ceiling probe (calibration, no data movement).
+ *   One CTA per SM issues `iters` tcgen05.mma kind::f16 instructions back to back: M = 128,
+ *   N = n (64, 128 or 256), K = 16, bf16 operands, fp32 accumulation in tensor memory.
+ *   mode 0: A and B from shared memory (the S = Q K^T form); mode 1: A from tensor memory (the
+ *   O += P V form); mode 2 (n = 128 only): the attention kernel's per-KV-step sequence of four
+ *   GEMMs with a commit after each, iters/32 steps; mode 3: as mode 2 with a
+ *   tcgen05.fence::after_thread_sync before each P*V GEMM; mode 4 (n = 128): iters/8 serial
+ *   round trips of one 128x128x128 GEMM -> commit -> a second warp waits, reads tensor memory
+ *   and arrives -> the issuing thread waits (hand-off latency); modes 5 / 6 / 7 (n = 128): mode
+ *   2 while four other warps stream tensor-memory loads and stores / run dependent FMA chains /
+ *   run independent FMA chains (contention).  The caller times the launch:
+ *   flops = SMs * iters * 2*128*n*16.  ATTN_ERR_INVALID_ARG for other arguments.
+ */
+CPATTN_API attn_status attn_probe_mma(int n, int mode, int iters, attn_stream_t stream);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 CPATTN_API int attn_version(void);
 
