@@ -19,6 +19,10 @@ def bits(t: torch.Tensor) -> np.ndarray:
 
 
 @pytest.mark.parametrize("P,B,S,H,D,dtype", [
+    (8, 2, 256, 32, 64, torch.float16),    # Ulysses-like (H/P = 4 heads per rank)
+    (4, 1, 512, 8, 128, torch.bfloat16),   # D = 128
+    (2, 1, 64, 4, 64, torch.float64),      # 8-byte elements
+    (2, 3, 48, 4, 8, torch.float16),       # batch 3
     (2, 1, 6, 4, 8, torch.float16),        # D*2 = 16 bytes: one vector per row
     (4, 3, 20, 8, 64, torch.bfloat16),
     (8, 2, 64, 16, 16, torch.float32),     # 4-byte elements
