@@ -15,7 +15,8 @@ import torch
 
 __all__ = ["CpAttnError", "CpAttnLibraryError", "lib", "attn_fwd", "attn_fwd_chunked",
            "attn_lse_merge", "cp_layout_seq2head", "cp_layout_head2seq", "attn_device_status",
-           "attn_watchdog_selftest", "attn_set_max_ctas", "attn_probe_mma", "attn_status_string", "attn_version",
+           "attn_watchdog_selftest", "attn_set_max_ctas", "attn_probe_mma",
+           "attn_set_kernel_variant", "attn_status_string", "attn_version",
            "LIB_PATH", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
            "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT"]
 
@@ -64,11 +65,13 @@ def lib() -> ctypes.CDLL:
     L.attn_device_status.argtypes = [vp]
     L.attn_watchdog_selftest.argtypes = [ctypes.c_uint64, vp]
     L.attn_set_max_ctas.argtypes = [i]
+    L.attn_set_kernel_variant.argtypes = [i]
     L.attn_probe_mma.argtypes = [i, i, i, vp]
     L.attn_version.argtypes = []
     for name in ("attn_fwd", "attn_fwd_chunked", "attn_lse_merge", "cp_layout_seq2head",
                  "cp_layout_head2seq", "attn_device_status", "attn_watchdog_selftest",
-                 "attn_set_max_ctas", "attn_version", "attn_probe_mma"):
+                 "attn_set_max_ctas", "attn_version", "attn_probe_mma",
+                 "attn_set_kernel_variant"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -84,6 +87,11 @@ def attn_version() -> int:
 
 def attn_set_max_ctas(n: int) -> int:
     return lib().attn_set_max_ctas(int(n))
+
+
+def attn_set_kernel_variant(v: int) -> int:
+    """0: single-CTA kernel (default); 1: D = 128 attention on SM pairs.  Returns the previous."""
+    return lib().attn_set_kernel_variant(int(v))
 
 
 def _stream(stream) -> Optional[int]:

@@ -34,6 +34,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <atomic>
 #include <mutex>
 
 #include "cpattn_internal.h"
@@ -132,16 +133,24 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[D]) {
   }
 }
 
-// One KV tile of the online softmax for this thread's row: read the 128 logits from TMEM,
-// update the running max m (only when it grows by more than the threshold; `need` reports a
-// move and `alpha` = 2^(m_old - m_new), or 1), write P = 2^(s*scale*log2e - m) as 16-bit pairs
-// over the first 64 columns of the same TMEM region, and return the row sum of P.  kMasked
-// treats columns >= valid as -inf (last tile of a KV chunk).
-template <bool BF16, bool kMasked>
-__device__ __forceinline__ float softmax_tile(uint32_t s_addr, float sl2, int valid, float& m,
-                                              bool& need, float& alpha) {
+// No-op hook for softmax_tile.
+struct NoHook {
+  __device__ __forceinline__ void operator()() const {}
+};
+
+// One KV tile of the online softmax for this thread's row: read the 128 logits from TMEM at
+// s_addr (then run after_load: the logits are in registers), update the running max m (only
+// when it grows by more than the threshold; `need` reports a move and `alpha` = 2^(m_old -
+// m_new), or 1), write P = 2^(s*scale*log2(e) - m) as 16-bit pairs to the 64 TMEM columns at
+// p_addr, and return the row sum of P.  kMasked treats columns >= valid as -inf (last tile of a
+// KV chunk).
+template <bool BF16, bool kMasked, typename AfterLoad = NoHook>
+__device__ __forceinline__ float softmax_tile(uint32_t s_addr, uint32_t p_addr, float sl2,
+                                              int valid, float& m, bool& need, float& alpha,
+                                              AfterLoad after_load = AfterLoad()) {
   uint32_t sr[kBN];
   ptx::tmem_ld128(s_addr, sr);
+  after_load();
   if constexpr (kMasked) {
 #pragma unroll
     for (int c = 0; c < kBN; ++c)
@@ -181,7 +190,7 @@ __device__ __forceinline__ float softmax_tile(uint32_t s_addr, float sl2, int va
       lacc[c & 3] = ptx::f2_add(lacc[c & 3], ptx::f2_pack(p0, p1));
       pk[c] = ptx::pack2<BF16>(p0, p1);
     }
-    ptx::tmem_st16(s_addr + 16 * h, pk);
+    ptx::tmem_st16(p_addr + 16 * h, pk);
   }
 #undef SV
   float la, lb;
@@ -433,8 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float alpha;
         const float l_tile =
             (j == w.n - 1 && w.last_valid < kBN)
-                ? softmax_tile<BF16, true>(s_addr, sl2, w.last_valid, m, need, alpha)
-                : softmax_tile<BF16, false>(s_addr, sl2, kBN, m, need, alpha);
+                ? softmax_tile<BF16, true>(s_addr, s_addr, sl2, w.last_valid, m, need, alpha)
+                : softmax_tile<BF16, false>(s_addr, s_addr, sl2, kBN, m, need, alpha);
         l = l * alpha + l_tile;
         // Rescale O (the P*V of earlier steps, whose MMAs completed before S_j was signalled)
         // when the max moved in any row of this warp.  P*V of this step is only issued after
@@ -492,6 +501,346 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+
+
+// ----------------------------------------------------------------------------- CTA-pair kernel
+// D = 128 variant that runs the tensor core in CTA pairs (cta_group::2, a cluster of two CTAs):
+// each MMA is M = 256 -- 128 query rows from each CTA -- and the B operand (a K tile for
+// S = Q K^T, a V tile for O += P V) is split along N between the two CTAs.  So each CTA loads
+// only half of every K/V tile (K: 64 of the 128 KV rows; V: 64 of the 128 columns of D) and
+// reads only its half from shared memory for the MMA: shared-memory traffic for B operands and
+// TMA writes per SM are halved, which is what limits the single-CTA kernel.
+//
+// Unit: (chunk, batch*head, 512-query block); CTA r of the pair owns query rows
+// [256 r, 256 r + 256) of the block as two 128-row tiles, exactly like the single-CTA kernel.
+// Roles per CTA as in the single-CTA kernel, plus warp 10 = relay: the even ("leader") CTA's
+// MMA thread issues for both CTAs, so it must know that both CTAs' operands have landed; each
+// CTA's relay thread waits for its own TMA completions and arrives on the leader's barriers.
+// Softmax warps of both CTAs publish P and release O on the leader's barriers (remote arrive
+// for the odd CTA); the leader's commits are multicast to the barriers of both CTAs.
+constexpr int kPairStages = 10;
+constexpr int kPairStageBytes = 16 * 1024;   // K half [64 rows][128 d] or V half [128 rows][64 d]
+constexpr int kPairQBytes = 128 * 128 * 2;   // one 128-row Q tile, D = 128
+constexpr int kRelayWarp = 10;
+constexpr int kPairNBars = 3 * kPairStages + 9 * kQT + 1;
+constexpr int kPairSmem =
+    1024 + kQT * kPairQBytes + kPairStages * kPairStageBytes + kPairNBars * 8 + 16;
+static_assert(kPairSmem <= 232448, "shared memory per CTA");
+
+template <bool BF16>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  constexpr int D = 128;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + kQT * kPairQBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + kPairStages * kPairStageBytes);
+  uint64_t* kv_full = bars;                        // local TMA completion
+  uint64_t* kv_empty = kv_full + kPairStages;      // leader commit (multicast)
+  uint64_t* kv_ready = kv_empty + kPairStages;     // leader only: both halves landed
+  uint64_t* q_full = kv_ready + kPairStages;
+  uint64_t* q_empty = q_full + kQT;
+  uint64_t* q_ready = q_empty + kQT;               // leader only
+  uint64_t* s_full = q_ready + kQT;
+  uint64_t* p_full = s_full + kQT;                 // leader only, 8 arrivals
+  uint64_t* o_full = p_full + kQT;
+  uint64_t* o_empty = o_full + kQT;                // leader only, 8 arrivals
+  uint64_t* mma_drain = o_empty + kQT;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kPairNBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint64_t lim = p.limit_ns;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const int cluster_id = static_cast<int>(blockIdx.x >> 1);
+  const int n_clusters = static_cast<int>(gridDim.x >> 1);
+  auto leader_addr = [&](const uint64_t* bar) { return ptx::mapa(ptx::smem_u32(bar), 0); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      ptx::mbar_init(&kv_full[s], 1);
+      ptx::mbar_init(&kv_empty[s], 1);
+      ptx::mbar_init(&kv_ready[s], 2);
+    }
+    for (int t = 0; t < kQT; ++t) {
+      ptx::mbar_init(&q_full[t], 1);
+      ptx::mbar_init(&q_empty[t], 1);
+      ptx::mbar_init(&q_ready[t], 2);
+      ptx::mbar_init(&s_full[t], 1);
+      ptx::mbar_init(&p_full[t], 8);
+      ptx::mbar_init(&o_full[t], 1);
+      ptx::mbar_init(&o_empty[t], 8);
+    }
+    ptx::mbar_init(mma_drain, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc_pair(tmem_slot, kTmemCols);
+    ptx::tmem_relinquish_pair();
+  }
+  if (warp == kLoaderWarp && lane == 0) {
+    ptx::prefetch_tmap(&tm_q);
+    ptx::prefetch_tmap(&tm_k);
+    ptx::prefetch_tmap(&tm_v);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();   // both CTAs' barriers exist before any remote arrive
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp >= 8) {
+    ptx::regs_dec<kProducerRegs>();
+    if (warp == kLoaderWarp && lane == 0) {
+      // ---------------------------------------------------------------- TMA producer (both)
+      uint32_t st = 0, ph = 0, it = 0, issued_total = 0;
+      int q_issued[kQT] = {-1, -1};
+      bool ok = true;
+      auto next_stage = [&](uint32_t& s_out, uint32_t& ph_out) -> bool {
+        s_out = st;
+        ph_out = ph;
+        if (++st == kPairStages) {
+          st = 0;
+          ph ^= 1;
+        }
+        return ptx::mbar_wait<true>(&kv_empty[s_out], ph_out ^ 1, abort_flag, &g_attn_status, lim);
+      };
+      for (int u = cluster_id; ok && u < p.num_units; u += n_clusters, ++it) {
+        const Unit w = decode_unit(u, p);
+        for (int t = 0; ok && t < kQT; ++t) {
+          ok = ptx::mbar_wait<true>(&q_empty[t], (it & 1) ^ 1, abort_flag, &g_attn_status, lim);
+          if (!ok) break;
+          q_issued[t] = static_cast<int>(it);
+          ptx::mbar_arrive_expect_tx(&q_full[t], kPairQBytes);
+          const int row = w.qb * (4 * kBM) + static_cast<int>(rank) * (kQT * kBM) + t * kBM;
+          for (int h = 0; h < 2; ++h)
+            ptx::tma_load_3d(sQ + t * kPairQBytes + h * kHalfBytes, &tm_q, 64 * h, row, w.bh,
+                             &q_full[t]);
+        }
+        for (int j = 0; ok && j < w.n; ++j) {
+          uint32_t s, sph;
+          // K: this CTA's 64 of the tile's 128 KV rows, both 64-column halves of D
+          if (!(ok = next_stage(s, sph))) break;
+          ptx::mbar_arrive_expect_tx(&kv_full[s], kPairStageBytes);
+          const int krow = w.lo + j * kBN + static_cast<int>(rank) * 64;
+          for (int h = 0; h < 2; ++h)
+            ptx::tma_load_3d(sKV + s * kPairStageBytes + h * (kPairStageBytes / 2), &tm_k, 64 * h,
+                             krow, w.bh, &kv_full[s]);
+          ++issued_total;
+          // V: all 128 KV rows, this CTA's 64 columns of D
+          if (!(ok = next_stage(s, sph))) break;
+          ptx::mbar_arrive_expect_tx(&kv_full[s], kPairStageBytes);
+          ptx::tma_load_3d(sKV + s * kPairStageBytes, &tm_v, 64 * static_cast<int>(rank),
+                           w.lo + j * kBN, w.bh, &kv_full[s]);
+          ++issued_total;
+        }
+      }
+      if (!ok) {
+        const uint32_t n = issued_total < kPairStages ? issued_total : kPairStages;
+        for (uint32_t i = issued_total - n; i < issued_total; ++i)
+          drain_wait(&kv_full[i % kPairStages], (i / kPairStages) & 1, lim);
+        for (int t = 0; t < kQT; ++t)
+          if (q_issued[t] >= 0) drain_wait(&q_full[t], q_issued[t] & 1, lim);
+      }
+    } else if (warp == kRelayWarp && lane == 0) {
+      // ---------------------------------------------------------------- relay (both CTAs)
+      uint32_t st = 0, ph = 0, it = 0;
+      bool ok = true;
+      for (int u = cluster_id; ok && u < p.num_units; u += n_clusters, ++it) {
+        const Unit w = decode_unit(u, p);
+        for (int t = 0; ok && t < kQT; ++t) {
+          ok = ptx::mbar_wait<true>(&q_full[t], it & 1, abort_flag, &g_attn_status, lim);
+          if (ok) ptx::mbar_arrive_cluster(leader_addr(&q_ready[t]));
+        }
+        for (int j = 0; ok && j < 2 * w.n; ++j) {
+          ok = ptx::mbar_wait<true>(&kv_full[st], ph, abort_flag, &g_attn_status, lim);
+          if (!ok) break;
+          ptx::mbar_arrive_cluster(leader_addr(&kv_ready[st]));
+          if (++st == kPairStages) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+      }
+    } else if (warp == kMmaWarp && lane == 0 && rank == 0) {
+      // ---------------------------------------------------------------- MMA issuer (leader)
+      constexpr uint32_t kIdescS = ptx::idesc_f16(BF16, false, 2 * kBM, kBN);
+      constexpr uint32_t kIdescPV = ptx::idesc_f16(BF16, true, 2 * kBM, D);
+      const uint32_t sQ_addr = ptx::smem_u32(sQ);
+      const uint32_t sKV_addr = ptx::smem_u32(sKV);
+      const uint32_t s_col[2] = {Cfg<D>::S_COL0, Cfg<D>::S_COL1};
+      const uint32_t o_col[2] = {Cfg<D>::O_COL0, Cfg<D>::O_COL1};
+      constexpr uint16_t kBoth = 0x3;
+
+      auto issue_s = [&](int t, uint32_t stg) {
+        const uint32_t a0 = sQ_addr + t * kPairQBytes;
+        const uint32_t b0 = sKV_addr + stg * kPairStageBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          ptx::mma_ss_pair(
+              tmem + s_col[t],
+              ptx::smem_desc_sw128(a0 + (ks >> 2) * kHalfBytes + (ks & 3) * 32, 16, 1024),
+              ptx::smem_desc_sw128(b0 + (ks >> 2) * (kPairStageBytes / 2) + (ks & 3) * 32, 16,
+                                   1024),
+              kIdescS, ks > 0);
+        }
+      };
+      auto issue_pv = [&](int t, uint32_t stg, bool acc) {
+        const uint32_t b0 = sKV_addr + stg * kPairStageBytes;
+#pragma unroll
+        for (int ks = 0; ks < kBN / 16; ++ks) {
+          ptx::mma_ts_pair(tmem + o_col[t], tmem + s_col[t] + ks * 8,
+                           ptx::smem_desc_sw128(b0 + ks * 2048, kHalfBytes, 1024), kIdescPV,
+                           (acc || ks > 0) ? 1u : 0u);
+        }
+      };
+
+      uint32_t kst = 0, kph = 0, it = 0, pph[2] = {0, 0};
+      bool ok = true;
+      auto wait_kv = [&](uint32_t& stg) -> bool {
+        stg = kst;
+        const uint32_t ph = kph;
+        if (++kst == kPairStages) {
+          kst = 0;
+          kph ^= 1;
+        }
+        return ptx::mbar_wait<true>(&kv_ready[stg], ph, abort_flag, &g_attn_status, lim);
+      };
+
+      for (int u = cluster_id; ok && u < p.num_units; u += n_clusters, ++it) {
+        const Unit w = decode_unit(u, p);
+        uint32_t sk, sv;
+        if (!(ok = wait_kv(sk))) break;
+        for (int t = 0; t < kQT; ++t) {
+          if (!(ok = ptx::mbar_wait<true>(&q_ready[t], it & 1, abort_flag, &g_attn_status, lim))) break;
+          ptx::tc_fence_after();
+          issue_s(t, sk);
+          ptx::mma_commit_pair(&s_full[t], kBoth);
+          if (w.n == 1) ptx::mma_commit_pair(&q_empty[t], kBoth);
+        }
+        if (!ok) break;
+        ptx::mma_commit_pair(&kv_empty[sk], kBoth);
+
+        for (int j = 1; ok && j <= w.n; ++j) {
+          if (!(ok = wait_kv(sv))) break;
+          for (int t = 0; t < kQT; ++t) {
+            if (!(ok = ptx::mbar_wait<true>(&p_full[t], pph[t], abort_flag, &g_attn_status, lim)))
+              break;
+            pph[t] ^= 1;
+            if (j == 1 && it > 0) {
+              if (!(ok = ptx::mbar_wait<true>(&o_empty[t], (it - 1) & 1, abort_flag, &g_attn_status,
+                                        lim)))
+                break;
+            }
+            ptx::tc_fence_after();
+            issue_pv(t, sv, j > 1);
+            if (t == kQT - 1) ptx::mma_commit_pair(&kv_empty[sv], kBoth);
+            if (j == w.n) {
+              ptx::mma_commit_pair(&o_full[t], kBoth);
+            } else {
+              if (t == 0 && !(ok = wait_kv(sk))) break;
+              issue_s(t, sk);
+              ptx::mma_commit_pair(&s_full[t], kBoth);
+              if (j == w.n - 1) ptx::mma_commit_pair(&q_empty[t], kBoth);
+              if (t == kQT - 1) ptx::mma_commit_pair(&kv_empty[sk], kBoth);
+            }
+          }
+        }
+      }
+      ptx::mma_commit_pair(mma_drain, 0x1);
+      drain_wait(mma_drain, 0, lim);
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax (both CTAs)
+    ptx::regs_inc<kSoftmaxRegs>();
+    const int t = warp >> 2;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t s_addr = tmem + lane_base + (t == 0 ? Cfg<D>::S_COL0 : Cfg<D>::S_COL1);
+    const uint32_t o_addr = tmem + lane_base + (t == 0 ? Cfg<D>::O_COL0 : Cfg<D>::O_COL1);
+    const uint32_t p_full_leader = leader_addr(&p_full[t]);
+    const uint32_t o_empty_leader = leader_addr(&o_empty[t]);
+    const float sl2 = p.scale_log2;
+    uint32_t sph = 0, oph = 0;
+    bool ok = true;
+
+    for (int u = cluster_id; ok && u < p.num_units; u += n_clusters) {
+      const Unit w = decode_unit(u, p);
+      float m = -INFINITY;
+      float l = 0.f;
+      for (int j = 0; j < w.n; ++j) {
+        ok = __all_sync(0xffffffffu,
+                        ptx::mbar_wait<true>(&s_full[t], sph, abort_flag, &g_attn_status, lim));
+        if (!ok) break;
+        sph ^= 1;
+        ptx::tc_fence_after();
+        bool need;
+        float alpha;
+        const float l_tile =
+            (j == w.n - 1 && w.last_valid < kBN)
+                ? softmax_tile<BF16, true>(s_addr, s_addr, sl2, w.last_valid, m, need, alpha)
+                : softmax_tile<BF16, false>(s_addr, s_addr, sl2, kBN, m, need, alpha);
+        l = l * alpha + l_tile;
+        if (j > 0 && __any_sync(0xffffffffu, need)) rescale_o<D>(o_addr, alpha);
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_cluster(p_full_leader);
+      }
+      if (!ok) break;
+
+      ok = __all_sync(0xffffffffu,
+                      ptx::mbar_wait<true>(&o_full[t], oph, abort_flag, &g_attn_status, lim));
+      if (!ok) break;
+      oph ^= 1;
+      ptx::tc_fence_after();
+      const int q_row = w.qb * (4 * kBM) + static_cast<int>(rank) * (kQT * kBM) + t * kBM + row;
+      const bool valid = q_row < p.Sq;
+      const float inv_l = 1.f / l;
+      const long long prow = static_cast<long long>(w.c) * p.BH + w.bh;
+      uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
+                       (prow * p.Sq + (valid ? q_row : 0)) * static_cast<long long>(D);
+#pragma unroll
+      for (int half = 0; half < D / 64; ++half) {
+        uint32_t orr[64];
+        ptx::tmem_ld64(o_addr + 64 * half, orr);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + 64 * half);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              pk[c] = ptx::pack2<BF16>(__uint_as_float(orr[8 * v + 2 * c]) * inv_l,
+                                       __uint_as_float(orr[8 * v + 2 * c + 1]) * inv_l);
+            dst[v] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+        }
+      }
+      if (valid && p.lse != nullptr)
+        p.lse[prow * p.Sq + q_row] = (m + __log2f(l)) * 0.69314718055994530942f;
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(o_empty_leader);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();   // the leader's MMAs on this CTA's memory are complete
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem, kTmemCols);
+  }
+}
+
 // Watchdog self-test: one thread waits on a barrier nobody arrives on.
 __global__ void watchdog_selftest_kernel(unsigned long long limit_ns) {
   __shared__ uint64_t bar;
@@ -522,21 +871,42 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
-// 3-D map over a [BH][S][D] 16-bit tensor, box = 64 elements x 128 rows x 1, 128-byte swizzle.
-bool make_map(CUtensorMap* map, const void* base, bool bf16, int D, int S, int BH) {
+// 3-D map over a [BH][S][D] 16-bit tensor, box = 64 elements x box_rows rows x 1, 128-byte
+// swizzle.
+bool make_map(CUtensorMap* map, const void* base, bool bf16, int D, int S, int BH,
+              int box_rows = 128) {
   auto enc = get_encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
                            static_cast<cuuint64_t>(S) * static_cast<cuuint64_t>(D) * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                    3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+template <bool BF16>
+cudaError_t launch_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                        const Params& p, int grid, cudaStream_t stream) {
+  auto kern = attn_fwd_pair_kernel<BF16>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  static int regs = -1;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
+    cudaFuncAttributes fa;
+    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, kern);
+    if (attr_err == cudaSuccess) regs = fa.numRegs;
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  if (regs != kLaunchRegs) return cudaErrorInvalidKernelImage;   // see the register split
+  kern<<<grid, kThreads, kPairSmem, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError();
 }
 
 template <int D, bool BF16>
@@ -569,12 +939,24 @@ int device_sm_count() {
   return n;
 }
 
+namespace {
+std::atomic<int> g_variant{0};
+}  // namespace
+
+int set_attention_variant(int v) { return g_variant.exchange(v); }
+
 attn_status launch_attention(const void* q, const void* k, const void* v, void* o, float* lse,
                              int P, int B, int H, int Sq, int Skv, int D, bool bf16, float scale,
                              cudaStream_t stream, unsigned long long limit_ns, int max_ctas) {
   const int BH = B * H;
+  int sms = device_sm_count();
+  if (sms <= 0) return ATTN_ERR_CUDA;
+  if (max_ctas > 0 && max_ctas < sms) sms = max_ctas;
+  // D = 128 runs on CTA pairs (needs at least one pair of SMs); D = 64 on single CTAs.
+  const bool pair = D == 128 && g_variant.load() == 1 && sms >= 2;
+  const int rows_per_unit = pair ? 4 * kBM : kQT * kBM;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, bf16, D, Sq, BH) || !make_map(&mk, k, bf16, D, Skv, BH) ||
+  if (!make_map(&mq, q, bf16, D, Sq, BH) || !make_map(&mk, k, bf16, D, Skv, BH, pair ? 64 : 128) ||
       !make_map(&mv, v, bf16, D, Skv, BH))
     return ATTN_ERR_CUDA;
   Params p;
@@ -582,7 +964,7 @@ attn_status launch_attention(const void* q, const void* k, const void* v, void* 
   p.Skv = Skv;
   p.P = P;
   p.BH = BH;
-  p.n_qb = (Sq + kQT * kBM - 1) / (kQT * kBM);
+  p.n_qb = (Sq + rows_per_unit - 1) / rows_per_unit;
   const long long units = static_cast<long long>(BH) * P * p.n_qb;
   if (units >= (1ll << 31) || P > 65536) return ATTN_ERR_UNSUPPORTED;
   p.num_units = static_cast<int>(units);
@@ -592,17 +974,20 @@ attn_status launch_attention(const void* q, const void* k, const void* v, void* 
   p.o = o;
   p.lse = lse;
   p.limit_ns = limit_ns;
-  int sms = device_sm_count();
-  if (sms <= 0) return ATTN_ERR_CUDA;
-  if (max_ctas > 0 && max_ctas < sms) sms = max_ctas;
-  const int grid = p.num_units < sms ? p.num_units : sms;
   cudaError_t e;
-  if (D == 128)
-    e = bf16 ? launch_typed<128, true>(mq, mk, mv, p, grid, stream)
-             : launch_typed<128, false>(mq, mk, mv, p, grid, stream);
-  else
-    e = bf16 ? launch_typed<64, true>(mq, mk, mv, p, grid, stream)
-             : launch_typed<64, false>(mq, mk, mv, p, grid, stream);
+  if (pair) {
+    const int pairs = p.num_units < sms / 2 ? p.num_units : sms / 2;
+    e = bf16 ? launch_pair<true>(mq, mk, mv, p, 2 * pairs, stream)
+             : launch_pair<false>(mq, mk, mv, p, 2 * pairs, stream);
+  } else {
+    const int grid = p.num_units < sms ? p.num_units : sms;
+    if (D == 128)
+      e = bf16 ? launch_typed<128, true>(mq, mk, mv, p, grid, stream)
+               : launch_typed<128, false>(mq, mk, mv, p, grid, stream);
+    else
+      e = bf16 ? launch_typed<64, true>(mq, mk, mv, p, grid, stream)
+               : launch_typed<64, false>(mq, mk, mv, p, grid, stream);
+  }
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

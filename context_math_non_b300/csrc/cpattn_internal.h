@@ -18,6 +18,10 @@ attn_status launch_attention(const void* q, const void* k, const void* v, void* 
                              int P, int B, int H, int Sq, int Skv, int D, bool bf16, float scale,
                              cudaStream_t stream, unsigned long long limit_ns, int max_ctas);
 
+// 1: D = 128 attention runs on CTA pairs; 0 (default): single-CTA kernel for every D.
+// Returns the previous setting.
+int set_attention_variant(int v);
+
 attn_status launch_lse_merge(const void* o_parts, const float* lse_parts, int P, long long rows,
                              int D, bool bf16, void* o, float* lse, cudaStream_t stream);
 

@@ -163,6 +163,15 @@ CPATTN_API int attn_set_max_ctas(int n);
  */
 CPATTN_API attn_status attn_probe_mma(int n, int mode, int iters, attn_stream_t stream);
 
+/*
+ * attn_set_kernel_variant -- choose the attention kernel for D = 128 (process-wide, affects later
+ *   launches): 0 (default) runs the single-CTA kernel; 1 runs it on pairs of SMs (cta_group::2
+ *   MMAs, each CTA loading half of every K/V tile -- measured slower on B300, kept for testing
+ *   and measurement).  D = 64 always uses the single-CTA kernel.  Both produce results within
+ *   the same tolerance.  Returns the previous setting.
+ */
+CPATTN_API int attn_set_kernel_variant(int v);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 CPATTN_API int attn_version(void);
 

@@ -61,6 +61,31 @@ def test_small_shapes(B, H, Sq, Skv, D, dtype, P):
     run_full_and_chunked(q, k, v, P, f"B{B} H{H} Sq{Sq} Skv{Skv} D{D} {dtype}")
 
 
+@pytest.mark.parametrize("B,H,Sq,Skv,D,dtype,P", [c for c in SMALL_CASES if c[4] == 128])
+def test_small_shapes_sm_pair_kernel(B, H, Sq, Skv, D, dtype, P):
+    """The same D = 128 cases on the CTA-pair kernel (cta_group::2; not the default)."""
+    prev = cpattn.attn_set_kernel_variant(1)
+    try:
+        q, k, v = rand_qkv(B, H, Sq, Skv, D, dtype, seed=Sq * 31 + Skv + P)
+        run_full_and_chunked(q, k, v, P, f"SM-pair B{B} H{H} Sq{Sq} Skv{Skv} {dtype}")
+    finally:
+        cpattn.attn_set_kernel_variant(prev)
+
+
+def test_pair_and_single_cta_kernels_agree():
+    """D = 128: the CTA-pair and single-CTA kernels give the same result to rounding."""
+    q, k, v = (t.cuda() for t in rand_qkv(1, 3, 1100, 900, 128, torch.bfloat16, seed=21))
+    o1, l1 = cpattn.attn_fwd_chunked(q, k, v, 3)
+    prev = cpattn.attn_set_kernel_variant(1)
+    try:
+        o2, l2 = cpattn.attn_fwd_chunked(q, k, v, 3)
+    finally:
+        cpattn.attn_set_kernel_variant(prev)
+    assert cpattn.attn_device_status() == cpattn.ATTN_OK
+    assert (o1.float() - o2.float()).abs().max().item() <= 2 ** -7
+    assert (l1 - l2).abs().max().item() <= 1e-4
+
+
 def test_large_logits_no_overflow():
     """Every logit lies around 90-100, where fp32 exp overflows without the running-max shift.
     Keys are shifted by a constant vector u (q has a positive mean), which moves each row's
@@ -75,11 +100,17 @@ def test_large_logits_no_overflow():
 
 
 def test_many_units_per_cta():
-    """A grid capped at 2 CTAs walks 36 units each: exercises every barrier phase wrap."""
+    """A grid capped at 2 CTAs (one SM pair) walks every unit of the problem: exercises every
+    barrier phase wrap, on both kernels."""
     q, k, v = rand_qkv(1, 3, 1000, 1000, 128, torch.bfloat16, seed=11)
     prev = cpattn.attn_set_max_ctas(2)
     try:
-        run_full_and_chunked(q, k, v, 3, "2 CTAs")
+        run_full_and_chunked(q, k, v, 3, "2 CTAs, single-CTA kernel")
+        pv = cpattn.attn_set_kernel_variant(1)
+        try:
+            run_full_and_chunked(q, k, v, 3, "2 CTAs, one SM pair")
+        finally:
+            cpattn.attn_set_kernel_variant(pv)
     finally:
         cpattn.attn_set_max_ctas(prev)
 
