@@ -250,6 +250,7 @@ def run_native(args, rank, world, local_rank):
                                            peaks["hbm_gbs"], 4)},
     }
     legs.update(_layout_leg(cpattn, dev, stream, peaks))
+    legs.update(_ulysses_leg(cpattn, dev, stream))
     clk = clocks.summary()
 
     e2e = None
@@ -440,6 +441,48 @@ def run_reference(args):
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
+
+
+def _ulysses_leg(cpattn, dev, stream, iters=5):
+    """Ulysses attention on [8][2][2048][32][64] fp16 (S = 16384, 32 heads): the fused kernel
+    (sequence-sharded addressing, no re-layout passes) against the unfused chain of
+    seq2head(Q, K, V) -> attention on [16][4][16384][64] -> head2seq(O)."""
+    w = WORKLOADS["ulysses"]
+    P, B, S, H, D = w.P[0], w.B, w.S, w.H, w.D
+    q, k, v = (t.to(dev) for t in draw_qkv(w))
+    o = torch.empty_like(q)
+    lse = torch.empty((P, B, H // P, S), dtype=torch.float32, device=dev)
+    qh, kh, vh, oh = (torch.empty((P * B, H // P, S, D), dtype=q.dtype, device=dev)
+                      for _ in range(4))
+    lh = torch.empty((P * B, H // P, S), dtype=torch.float32, device=dev)
+
+    def fused():
+        cpattn.attn_fwd_ulysses(q, k, v, o, lse, stream=stream)
+
+    def chain():
+        for x, y in ((q, qh), (k, kh), (v, vh)):
+            cpattn.cp_layout_seq2head(x, y.view(P, B, H // P, S, D), stream=stream)
+        cpattn.attn_fwd(qh, kh, vh, oh, lh, stream=stream)
+        cpattn.cp_layout_head2seq(oh.view(P, B, H // P, S, D), o, stream=stream)
+
+    flops = 4.0 * B * H * S * S * D
+    out = {}
+    for name, fn in (("fused", fused), ("unfused_chain", chain)):
+        fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(iters)]
+        for a, b in evs:
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+        out[name] = {"median_ms": round(ms, 4), "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1)}
+    st = cpattn.attn_device_status(stream)
+    if st != cpattn.ATTN_OK:
+        raise RuntimeError(f"device status after Ulysses leg: {cpattn.attn_status_string(st)}")
+    del q, k, v, o, lse, qh, kh, vh, oh, lh
+    return {"ulysses_attention": out}
 
 
 def run_profile_case(args):

@@ -84,10 +84,54 @@ struct Params {
   int num_units;     // BH * P * n_qb (< 2^31, checked on the host)
   int kv_q, kv_r;    // Skv = kv_q * P + kv_r
   float scale_log2;
-  void* o;           // [P][BH][Sq][D]
+  void* o;           // [P][BH][Sq][D]  (sequence-sharded layout: see SeqLayout)
   float* lse;        // [P][BH][Sq] or null
   unsigned long long limit_ns;
+  // Sequence-sharded (Ulysses) addressing, used by the kSeq kernels only: Q/K/V/O are
+  // [R][B][S/R][H][D] for R ranks; attention head bh = (g*B + b)*(H/R) + j is head g*(H/R) + j
+  // of batch b, and token t = r*(S/R) + s lives in rank r's shard.
+  int sq_R, sq_B, sq_H, sq_Hl, sq_Sl, sq_box;
 };
+
+// Rows [row, row + 128) of head bh into one 64-column half of a swizzled tile.  The plain layout
+// is one 3-D box; the sequence-sharded layout takes boxes of sq_box rows (never straddling two
+// ranks' shards) from the 4-D map (D, H, S/R, R*B).  Rows past the end are zero-filled by TMA.
+template <bool kSeq>
+__device__ __forceinline__ void load_rows(uint8_t* dst, const CUtensorMap* map, int x, int row,
+                                          int bh, uint64_t* bar, const Params& p) {
+  if constexpr (!kSeq) {
+    ptx::tma_load_3d(dst, map, x, row, bh, bar);
+  } else {
+    const int j = bh % p.sq_Hl;
+    const int rb = bh / p.sq_Hl;
+    const int b = rb % p.sq_B;
+    const int g = rb / p.sq_B;
+    const int h = g * p.sq_Hl + j;
+    for (int r0 = 0; r0 < 128; r0 += p.sq_box) {
+      const int t = row + r0;
+      const int rank = t / p.sq_Sl;
+      ptx::tma_load_4d(dst + r0 * 128, map, x, h, t - rank * p.sq_Sl, rank * p.sq_B + b, bar);
+    }
+  }
+}
+
+// Element offset of output row q_row of head bh (partial prow) in O.
+template <bool kSeq, int D>
+__device__ __forceinline__ long long out_row_offset(long long prow, int bh, int q_row,
+                                                    const Params& p) {
+  if constexpr (!kSeq) {
+    return (prow * p.Sq + q_row) * static_cast<long long>(D);
+  } else {
+    const int j = bh % p.sq_Hl;
+    const int rb = bh / p.sq_Hl;
+    const int b = rb % p.sq_B;
+    const int g = rb / p.sq_B;
+    const int rank = q_row / p.sq_Sl;
+    const long long tok = (static_cast<long long>(rank) * p.sq_B + b) * p.sq_Sl +
+                          (q_row - rank * p.sq_Sl);
+    return (tok * p.sq_H + g * p.sq_Hl + j) * static_cast<long long>(D);
+  }
+}
 
 struct Unit {
   int qb, c, bh, lo, n, last_valid;
@@ -226,7 +270,7 @@ __device__ __forceinline__ void rescale_o(uint32_t o_addr, float alpha) {
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool kSeq>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -303,8 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           q_issued[t] = static_cast<int>(it);
           ptx::mbar_arrive_expect_tx(&q_full[t], C::TILE);
           for (int h = 0; h < C::NH; ++h)
-            ptx::tma_load_3d(sQ + t * C::TILE + h * kHalfBytes, &tm_q, 64 * h,
-                             w.qb * (kQT * kBM) + t * kBM, w.bh, &q_full[t]);
+            load_rows<kSeq>(sQ + t * C::TILE + h * kHalfBytes, &tm_q, 64 * h,
+                            w.qb * (kQT * kBM) + t * kBM, w.bh, &q_full[t], p);
         }
         for (int j = 0; ok && j < w.n; ++j) {
           for (int which = 0; which < 2; ++which) {
@@ -315,8 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_arrive_expect_tx(&kv_full[st], C::TILE);
             const CUtensorMap* map = which == 0 ? &tm_k : &tm_v;
             for (int h = 0; h < C::NH; ++h)
-              ptx::tma_load_3d(sKV + st * C::TILE + h * kHalfBytes, map, 64 * h,
-                               w.lo + j * kBN, w.bh, &kv_full[st]);
+              load_rows<kSeq>(sKV + st * C::TILE + h * kHalfBytes, map, 64 * h,
+                              w.lo + j * kBN, w.bh, &kv_full[st], p);
             ++kv_pos;
           }
         }
@@ -467,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv_l = 1.f / l;
       const long long prow = static_cast<long long>(w.c) * p.BH + w.bh;
       uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
-                       (prow * p.Sq + (valid ? q_row : 0)) * static_cast<long long>(D);
+                       out_row_offset<kSeq, D>(prow, w.bh, valid ? q_row : 0, p);
 #pragma unroll
       for (int half = 0; half < D / 64; ++half) {
         uint32_t orr[64];
@@ -909,10 +953,10 @@ cudaError_t launch_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
   return cudaGetLastError();
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool kSeq = false>
 cudaError_t launch_typed(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const Params& p, int grid, cudaStream_t stream) {
-  auto kern = attn_fwd_kernel<D, BF16>;
+  auto kern = attn_fwd_kernel<D, BF16, kSeq>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int regs = -1;
@@ -988,6 +1032,75 @@ attn_status launch_attention(const void* q, const void* k, const void* v, void* 
       e = bf16 ? launch_typed<64, true>(mq, mk, mv, p, grid, stream)
                : launch_typed<64, false>(mq, mk, mv, p, grid, stream);
   }
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+namespace {
+// 4-D map over a sequence-sharded [R][B][S/R][H][D] 16-bit tensor as (D, H, S/R, R*B), box =
+// 64 elements x 1 head x box_rows tokens x 1, 128-byte swizzle.
+bool make_seq_map(CUtensorMap* map, const void* base, bool bf16, int D, int H, int Sl, int RB,
+                  int box_rows) {
+  auto enc = get_encode_fn();
+  if (!enc) return false;
+  const cuuint64_t e = 2;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(Sl), static_cast<cuuint64_t>(RB)};
+  cuuint64_t strides[3] = {D * e, static_cast<cuuint64_t>(H) * D * e,
+                           static_cast<cuuint64_t>(Sl) * H * D * e};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
+attn_status launch_attention_ulysses(const void* q, const void* k, const void* v, void* o,
+                                     float* lse, int R, int B, int S, int H, int D, bool bf16,
+                                     float scale, cudaStream_t stream,
+                                     unsigned long long limit_ns, int max_ctas) {
+  const int Sl = S / R, Hl = H / R;
+  int box = 128;
+  while (box >= 16 && Sl % box != 0) box >>= 1;
+  if (box < 16) return ATTN_ERR_UNSUPPORTED;
+  CUtensorMap mq, mk, mv;
+  if (!make_seq_map(&mq, q, bf16, D, H, Sl, R * B, box) ||
+      !make_seq_map(&mk, k, bf16, D, H, Sl, R * B, box) ||
+      !make_seq_map(&mv, v, bf16, D, H, Sl, R * B, box))
+    return ATTN_ERR_CUDA;
+  int sms = device_sm_count();
+  if (sms <= 0) return ATTN_ERR_CUDA;
+  if (max_ctas > 0 && max_ctas < sms) sms = max_ctas;
+  Params p;
+  p.Sq = S;
+  p.Skv = S;
+  p.P = 1;
+  p.BH = B * H;                      // R*B*(H/R) attention heads
+  p.n_qb = (S + kQT * kBM - 1) / (kQT * kBM);
+  const long long units = static_cast<long long>(p.BH) * p.n_qb;
+  if (units >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+  p.num_units = static_cast<int>(units);
+  p.kv_q = S;
+  p.kv_r = 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.o = o;
+  p.lse = lse;
+  p.limit_ns = limit_ns;
+  p.sq_R = R;
+  p.sq_B = B;
+  p.sq_H = H;
+  p.sq_Hl = Hl;
+  p.sq_Sl = Sl;
+  p.sq_box = box;
+  const int grid = p.num_units < sms ? p.num_units : sms;
+  cudaError_t e;
+  if (D == 128)
+    e = bf16 ? launch_typed<128, true, true>(mq, mk, mv, p, grid, stream)
+             : launch_typed<128, false, true>(mq, mk, mv, p, grid, stream);
+  else
+    e = bf16 ? launch_typed<64, true, true>(mq, mk, mv, p, grid, stream)
+             : launch_typed<64, false, true>(mq, mk, mv, p, grid, stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

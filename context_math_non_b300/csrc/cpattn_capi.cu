@@ -105,6 +105,30 @@ attn_status attn_fwd_chunked(const void* q, const void* k, const void* v, int P,
                                   cpattn::kDefaultWaitLimitNs, g_max_ctas.load());
 }
 
+attn_status attn_fwd_ulysses(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int P, int B, int S, int H, int D, attn_dtype dt, float scale,
+                             attn_stream_t stream) {
+  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  if (P < 1 || B < 0 || S < 0 || H < 0 || D < 1 || !valid_dtype(dt)) return ATTN_ERR_INVALID_ARG;
+  if (S % P != 0 || H % P != 0) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H > INT_MAX) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(o) || misaligned(lse))
+    return ATTN_ERR_MISALIGNED;
+  if (B == 0 || H == 0 || S == 0) return ATTN_OK;
+  if ((S / P) % 16 != 0) return ATTN_ERR_UNSUPPORTED;
+  const long long bytes = static_cast<long long>(B) * S * H * D * 2;
+  const long long lbytes = static_cast<long long>(B) * S * H * 4;
+  for (const void* in : {q, k, v})
+    if (overlaps(o, bytes, in, bytes) || overlaps(lse, lbytes, in, bytes))
+      return ATTN_ERR_INVALID_ARG;
+  if (overlaps(o, bytes, lse, lbytes)) return ATTN_ERR_INVALID_ARG;
+  return cpattn::launch_attention_ulysses(q, k, v, o, lse, P, B, S, H, D, dt == ATTN_BF16,
+                                          resolve_scale(scale, D),
+                                          reinterpret_cast<cudaStream_t>(stream),
+                                          cpattn::kDefaultWaitLimitNs, g_max_ctas.load());
+}
+
 attn_status attn_lse_merge(const void* o_parts, const float* lse_parts, int P, int B, int H,
                            int Sq, int D, attn_dtype dt, void* o, float* lse,
                            attn_stream_t stream) {

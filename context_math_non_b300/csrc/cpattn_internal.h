@@ -22,6 +22,13 @@ attn_status launch_attention(const void* q, const void* k, const void* v, void* 
 // Returns the previous setting.
 int set_attention_variant(int v);
 
+// Ulysses attention reading Q/K/V and writing O in the sequence-sharded layout
+// [R][B][S/R][H][D] (R = rank count); LSE in the head-sharded order [R][B][H/R][S].
+attn_status launch_attention_ulysses(const void* q, const void* k, const void* v, void* o,
+                                     float* lse, int R, int B, int S, int H, int D, bool bf16,
+                                     float scale, cudaStream_t stream,
+                                     unsigned long long limit_ns, int max_ctas);
+
 attn_status launch_lse_merge(const void* o_parts, const float* lse_parts, int P, long long rows,
                              int D, bool bf16, void* o, float* lse, cudaStream_t stream);
 

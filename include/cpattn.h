@@ -119,6 +119,24 @@ CPATTN_API attn_status cp_layout_seq2head(const void* in, void* out, int P, int 
 CPATTN_API attn_status cp_layout_head2seq(const void* in, void* out, int P, int B, int S, int H, int D,
                                int elem_bytes, attn_stream_t stream);
 
+/*
+ * attn_fwd_ulysses -- DeepSpeed Ulysses attention without the two re-layout passes.
+ *   Defines: page subsection "DeepSpeed Ulysses" and Figure 4 -- after the first all-to-all each
+ *   rank attends over the full sequence for its subset of heads, and the second all-to-all
+ *   returns the output to sequence sharding.  Here both all-to-alls are folded into the
+ *   attention kernel's addressing: Q, K, V are read and O is written in the sequence-sharded
+ *   layout, and the result equals
+ *     cp_layout_head2seq(attn_fwd(cp_layout_seq2head(q), cp_layout_seq2head(k),
+ *                                 cp_layout_seq2head(v)))  (attention per head, full sequence).
+ *   q, k, v, o [P][B][S/P][H][D]  dtype `dt`   (rank p holds tokens p*S/P .. (p+1)*S/P - 1)
+ *   lse        [P][B][H/P][S] fp32, written if non-NULL (rank g, batch b, head g*H/P + j, token t)
+ *   Requires S % P == 0, H % P == 0, (S/P) % 16 == 0 (ATTN_ERR_UNSUPPORTED otherwise: token tiles
+ *   are gathered in boxes that never straddle two ranks' shards), D = 64 or 128.
+ */
+CPATTN_API attn_status attn_fwd_ulysses(const void* q, const void* k, const void* v, void* o,
+                                        float* lse, int P, int B, int S, int H, int D,
+                                        attn_dtype dt, float scale, attn_stream_t stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 CPATTN_API const char* attn_status_string(attn_status status);
 

@@ -216,3 +216,18 @@ def head2seq(y, P: int) -> np.ndarray:
     x = y.reshape(P, B, Hl, P, Sl, D)          # [g][b][j][p][s][d]
     x = x.transpose(3, 1, 4, 0, 2, 5)          # [p][b][s][g][j][d]
     return np.ascontiguousarray(x.reshape(P, B, Sl, P * Hl, D))
+
+
+def ulysses_attention(q, k, v, P: int, scale: float | None = None):
+    """DeepSpeed Ulysses attention on sequence-sharded inputs, as the page's "DeepSpeed Ulysses"
+    subsection (Figure 4) lays it out: all-to-all to head sharding, full-sequence attention per
+    head on every rank, all-to-all back to sequence sharding.
+
+    q, k, v [P][B][S/P][H][D] -> O [P][B][S/P][H][D] (float64), LSE [P][B][H/P][S] (rank g
+    holds heads g*H/P .. (g+1)*H/P - 1, every token in global order).
+    """
+    qh, kh, vh = (seq2head(to_f64(t), P) for t in (q, k, v))
+    Pg, B, Hl, S, D = qh.shape
+    o, lse = attention(qh.reshape(Pg * B, Hl, S, D), kh.reshape(Pg * B, Hl, S, D),
+                       vh.reshape(Pg * B, Hl, S, D), scale)
+    return head2seq(o.reshape(Pg, B, Hl, S, D), P), lse.reshape(Pg, B, Hl, S)

@@ -40,8 +40,8 @@ def L_():
 
 def test_header_declares_the_boundary():
     fns = declared_functions()
-    for name in ("attn_fwd", "attn_fwd_chunked", "attn_lse_merge", "cp_layout_seq2head",
-                 "cp_layout_head2seq", "attn_status_string", "attn_device_status",
+    for name in ("attn_fwd", "attn_fwd_chunked", "attn_lse_merge", "attn_fwd_ulysses",
+                 "cp_layout_seq2head", "cp_layout_head2seq", "attn_status_string", "attn_device_status",
                  "attn_watchdog_selftest"):
         assert name in fns, name
 
@@ -142,3 +142,23 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(cpattn, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(cpattn.CpAttnLibraryError):
         cpattn.lib()
+
+
+def uly(L_, q=A, k=B_, v=C, o=O, lse=L, P=4, B=1, S=512, H=8, D=64, dt=0):
+    return L_.attn_fwd_ulysses(q, k, v, o, lse, P, B, S, H, D, dt, 0.0, None)
+
+
+def test_ulysses_argument_errors(L_):
+    E, U, M = cpattn.ATTN_ERR_INVALID_ARG, cpattn.ATTN_ERR_UNSUPPORTED, cpattn.ATTN_ERR_MISALIGNED
+    assert uly(L_, q=None) == E
+    assert uly(L_, P=0) == E
+    assert uly(L_, S=510) == E                      # S not divisible by P
+    assert uly(L_, H=6) == E                        # H not divisible by P
+    assert uly(L_, dt=2) == E
+    assert uly(L_, D=96) == U
+    assert uly(L_, S=4 * 24) == U                   # S/P = 24 is not a multiple of 16
+    assert uly(L_, v=C + 8) == M
+    assert uly(L_, o=B_ + 4096) == E                # output inside k
+    assert uly(L_, lse=O + 64) == E                 # lse inside o
+    assert uly(L_, B=0) == cpattn.ATTN_OK           # empty problems touch nothing
+    assert uly(L_, S=0) == cpattn.ATTN_OK

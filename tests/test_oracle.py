@@ -311,6 +311,28 @@ def test_layout_preserves_bits_of_16bit_types():
     np.testing.assert_array_equal(oracle.head2seq(y, 2), bits)
 
 
+def pin_ulysses(fn):
+    """Ulysses is exact: sharding the sequence, swapping to head sharding and back gives, for
+    every token and head, plain full-sequence attention over the unsharded tensor (torch SDPA in
+    float64 here), with the LSE of head g*H/P + j at rank g."""
+    P, B, Sl, H, D = 2, 2, 3, 4, 5
+    g = torch.Generator().manual_seed(11)
+    q, k, v = (torch.randn(P, B, Sl, H, D, generator=g, dtype=torch.float64) for _ in range(3))
+    # unshard: [P][B][Sl][H][D] -> [B][H][S][D] with token p*Sl + s
+    full = [t.permute(1, 3, 0, 2, 4).reshape(B, H, P * Sl, D) for t in (q, k, v)]
+    ref = torch.nn.functional.scaled_dot_product_attention(*full, is_causal=False)
+    lse_ref = torch.logsumexp(full[0] @ full[1].transpose(-1, -2) / math.sqrt(D), dim=-1)
+    ref_seq = ref.reshape(B, H, P, Sl, D).permute(2, 0, 3, 1, 4)          # [P][B][Sl][H][D]
+    lse_head = lse_ref.reshape(B, P, H // P, P * Sl).permute(1, 0, 2, 3)   # [P][B][Hl][S]
+    o, lse = fn(q.numpy(), k.numpy(), v.numpy(), P)
+    np.testing.assert_allclose(o, ref_seq.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_head.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_ulysses_equals_unsharded_attention():
+    pin_ulysses(oracle.ulysses_attention)
+
+
 def test_raw_fp32_and_rounded_inputs_agree_to_bf16_precision():
     """tiny workload: the fp32 draw and its bf16 rounding give outputs within bf16 input error."""
     from context_math_non_b300.inputs import WORKLOADS, draw_qkv
@@ -402,6 +424,20 @@ def _mutants():
         y = x.reshape(P, B, Sl, H // P, P, D).transpose(4, 1, 3, 0, 2, 5)
         return np.ascontiguousarray(y.reshape(P, B, H // P, P * Sl, D))
 
+    def ulysses_local_only(q, k, v, P):
+        # no all-to-all: each rank attends over its own tokens only
+        q, k, v = (np.asarray(t) for t in (q, k, v))
+        Pi, B, Sl, H, D = q.shape
+        tr = lambda t: t.transpose(0, 1, 3, 2, 4).reshape(P * B, H, Sl, D)
+        o, lse = oracle.attention(tr(q), tr(k), tr(v))
+        o = o.reshape(P, B, H, Sl, D).transpose(0, 1, 3, 2, 4)
+        return o, np.zeros((P, B, H // P, P * Sl))
+
+    def ulysses_lse_batch_major(q, k, v, P):
+        # LSE returned [B][P][H/P][S] instead of rank-major
+        o, lse = oracle.ulysses_attention(q, k, v, P)
+        return o, np.ascontiguousarray(lse.transpose(1, 0, 2, 3))
+
     return [
         ("attention: no scale", lambda: pin_torch_sdpa(no_scale)),
         ("attention: transposed V", lambda: pin_bruteforce(transposed_v)),
@@ -417,6 +453,8 @@ def _mutants():
             oracle.attention, oracle.attention_chunked, oracle.lse_merge, online_no_correction)),
         ("layout: swapped indices", lambda: pin_layout(s2h_swapped, oracle.head2seq)),
         ("layout: strided head split", lambda: pin_layout(s2h_head_order, oracle.head2seq)),
+        ("ulysses: local attention only", lambda: pin_ulysses(ulysses_local_only)),
+        ("ulysses: batch-major LSE", lambda: pin_ulysses(ulysses_lse_batch_major)),
     ]
 
 
