@@ -546,6 +546,13 @@ def run_mma_probe():
     for mode, label in labels.items():
         ms = rate(128, mode, 64000)
         out[label] = round(sms * 64000 * 2 * 128 * 128 * 16 / ms / 1e9, 1)
+    for mode, label, D in ((8, "d64_step_sequence_one_lane", 64),
+                           (9, "d64_step_sequence_converged_warp_elect", 64),
+                           (10, "d128_step_sequence_converged_warp_elect", 128)):
+        per_step = 2 * (8 + D // 16)
+        steps = 48000 // per_step
+        ms = rate(128, mode, steps * per_step)
+        out[label] = round(sms * steps * 2 * 4 * 128 * 128 * D / ms / 1e9, 1)
     ms = rate(128, 4, 32000)
     out["handoff_round_trip_ns"] = round(ms * 1e6 / 4000, 1)
     out["gemm_128x128x128_ns_at_peak"] = round(2 * 128 ** 3 / (2.26e15 / sms) * 1e9, 1)

@@ -376,31 +376,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop with identical control flow (every wait is voted across
+    // the warp); one elected lane issues each MMA and commit.
+    {
       constexpr uint32_t kIdescS = ptx::idesc_f16(BF16, false, kBM, kBN);
       constexpr uint32_t kIdescPV = ptx::idesc_f16(BF16, true, kBM, D);
       const uint32_t sQ_addr = ptx::smem_u32(sQ);
       const uint32_t sKV_addr = ptx::smem_u32(sKV);
-      const uint32_t s_col[2] = {C::S_COL0, C::S_COL1};
-      const uint32_t o_col[2] = {C::O_COL0, C::O_COL1};
 
       auto issue_s = [&](int t, uint32_t st) {
         const uint32_t a0 = sQ_addr + t * C::TILE;
         const uint32_t b0 = sKV_addr + st * C::TILE;
+        const uint32_t d_s = tmem + (t == 0 ? C::S_COL0 : C::S_COL1);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-          ptx::mma_ss(tmem + s_col[t], ptx::smem_desc_sw128(a0 + off, 16, 1024),
-                      ptx::smem_desc_sw128(b0 + off, 16, 1024), kIdescS, ks > 0);
+          ptx::mma_ss_elect(d_s, ptx::smem_desc_sw128(a0 + off, 16, 1024),
+                            ptx::smem_desc_sw128(b0 + off, 16, 1024), kIdescS, ks > 0);
         }
       };
       auto issue_pv = [&](int t, uint32_t st, bool acc) {
         const uint32_t b0 = sKV_addr + st * C::TILE;
+        const uint32_t d_o = tmem + (t == 0 ? C::O_COL0 : C::O_COL1);
+        const uint32_t a_p = tmem + (t == 0 ? C::S_COL0 : C::S_COL1);
 #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks) {
-          ptx::mma_ts(tmem + o_col[t], tmem + s_col[t] + ks * 8,
-                      ptx::smem_desc_sw128(b0 + ks * 2048, kHalfBytes, 1024), kIdescPV,
-                      (acc || ks > 0) ? 1u : 0u);
+          ptx::mma_ts_elect(d_o, a_p + ks * 8,
+                            ptx::smem_desc_sw128(b0 + ks * 2048, kHalfBytes, 1024), kIdescPV,
+                            (acc || ks > 0) ? 1u : 0u);
         }
       };
 
@@ -410,7 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         st = kv_pos % C::STAGES;
         const uint32_t ph = (kv_pos / C::STAGES) & 1;
         ++kv_pos;
-        return ptx::mbar_wait(&kv_full[st], ph, abort_flag, &g_attn_status, lim);
+        return __all_sync(0xffffffffu,
+                          ptx::mbar_wait(&kv_full[st], ph, abort_flag, &g_attn_status, lim));
       };
 
       for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
@@ -418,43 +422,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sk, sv;
         if (!(ok = wait_kv(sk))) break;
         for (int t = 0; t < kQT; ++t) {
-          if (!(ok = ptx::mbar_wait(&q_full[t], it & 1, abort_flag, &g_attn_status, lim))) break;
+          if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(&q_full[t], it & 1, abort_flag,
+                                                             &g_attn_status, lim))))
+            break;
           ptx::tc_fence_after();
           issue_s(t, sk);
-          ptx::mma_commit(&s_full[t]);
-          if (w.n == 1) ptx::mma_commit(&q_empty[t]);
+          ptx::mma_commit_elect(&s_full[t]);
+          if (w.n == 1) ptx::mma_commit_elect(&q_empty[t]);
         }
         if (!ok) break;
-        ptx::mma_commit(&kv_empty[sk]);
+        ptx::mma_commit_elect(&kv_empty[sk]);
 
         for (int j = 1; ok && j <= w.n; ++j) {
           if (!(ok = wait_kv(sv))) break;
           for (int t = 0; t < kQT; ++t) {
-            if (!(ok = ptx::mbar_wait(&p_full[t], pph[t], abort_flag, &g_attn_status, lim)))
+            if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(&p_full[t], pph[t], abort_flag,
+                                                               &g_attn_status, lim))))
               break;
             pph[t] ^= 1;
             if (j == 1 && it > 0) {
-              if (!(ok = ptx::mbar_wait(&o_empty[t], (it - 1) & 1, abort_flag, &g_attn_status,
-                                        lim)))
+              if (!(ok = __all_sync(0xffffffffu,
+                                    ptx::mbar_wait(&o_empty[t], (it - 1) & 1, abort_flag,
+                                                   &g_attn_status, lim))))
                 break;
             }
             ptx::tc_fence_after();
             issue_pv(t, sv, j > 1);
-            if (t == kQT - 1) ptx::mma_commit(&kv_empty[sv]);
+            if (t == kQT - 1) ptx::mma_commit_elect(&kv_empty[sv]);
             if (j == w.n) {
-              ptx::mma_commit(&o_full[t]);
+              ptx::mma_commit_elect(&o_full[t]);
             } else {
               if (t == 0 && !(ok = wait_kv(sk))) break;
               issue_s(t, sk);
-              ptx::mma_commit(&s_full[t]);
-              if (j == w.n - 1) ptx::mma_commit(&q_empty[t]);
-              if (t == kQT - 1) ptx::mma_commit(&kv_empty[sk]);
+              ptx::mma_commit_elect(&s_full[t]);
+              if (j == w.n - 1) ptx::mma_commit_elect(&q_empty[t]);
+              if (t == kQT - 1) ptx::mma_commit_elect(&kv_empty[sk]);
             }
           }
         }
       }
-      // All MMAs this thread issued complete before TMEM is released.
-      ptx::mma_commit(mma_drain);
+      // All MMAs this warp issued complete before TMEM is released.
+      ptx::mma_commit_elect(mma_drain);
       drain_wait(mma_drain, 0, lim);
     }
   }

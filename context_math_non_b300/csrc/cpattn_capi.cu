@@ -190,7 +190,7 @@ attn_status attn_watchdog_selftest(uint64_t limit_ns, attn_stream_t stream) {
 }
 
 attn_status attn_probe_mma(int n, int mode, int iters, attn_stream_t stream) {
-  if ((n != 64 && n != 128 && n != 256) || mode < 0 || mode > 7 || iters < 1)
+  if ((n != 64 && n != 128 && n != 256) || mode < 0 || mode > 10 || iters < 1)
     return ATTN_ERR_INVALID_ARG;
   if (mode >= 2 && n != 128) return ATTN_ERR_INVALID_ARG;
   return cpattn::launch_mma_probe(n, mode, iters, reinterpret_cast<cudaStream_t>(stream));

@@ -26,7 +26,10 @@ constexpr int kProbeSmem = 2 * 128 * 256 * 2 + 1024;   // A and B operand space 
 // second barrier, which the MMA thread waits for before the next GEMM (serial round trips);
 // 5 = step pattern while warps 4-7 stream tensor-memory loads (128 columns) and stores (64
 // columns) like the softmax does; 6 = step pattern while warps 4-7 run dependent FMA chains;
-// 7 = the same with eight independent FMA chains per thread (issue-bound background).
+// 7 = the same with eight independent FMA chains per thread (issue-bound background);
+// 8 = the D = 64 per-step sequence (per query tile: 8 TS MMAs N = 64 for P*V, 4 SS MMAs N = 128
+// K = 16 for Q*K^T, one commit) issued by one lane; 9 = the same issued by a converged warp
+// through elect.sync; 10 = the D = 128 step sequence (mode 2) issued by a converged warp.
 template <int N, int kMode>
 __global__ void __launch_bounds__(256, 1) mma_probe_kernel(int iters) {
   constexpr bool kTS = kMode == 1;
@@ -95,6 +98,46 @@ __global__ void __launch_bounds__(256, 1) mma_probe_kernel(int iters) {
         __syncwarp();
         if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(&ping);
         if (v[0] == 0xFFFFFFFFu && v[31] == 0x12345678u) abort_flag = 1;   // keep the load
+      }
+    }
+  } else if constexpr (kMode >= 8) {
+    // issue-path comparison: warp 0, either lane 0 alone (8) or all lanes with elect.sync
+    constexpr bool kWarp = kMode >= 9;
+    constexpr int Dh = kMode == 10 ? 128 : 64;
+    if (threadIdx.x < 32 && (kWarp || threadIdx.x == 0)) {
+      const uint32_t a_addr = ptx::smem_u32(smem);
+      const uint32_t b_addr = a_addr + 128 * 256 * 2;
+      constexpr uint32_t idS = ptx::idesc_f16(true, false, 128, 128);
+      constexpr uint32_t idPV = ptx::idesc_f16(true, true, 128, Dh);
+      constexpr int kPerStep = 2 * (8 + Dh / 16);
+      for (int i = 0; i < iters / kPerStep; ++i) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const uint32_t d_o = tmem + 256 + t * Dh, a_p = tmem + 128 * t;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint64_t bd = ptx::smem_desc_sw128(b_addr + 16384 + ks * 2048, 16384, 1024);
+            if constexpr (kWarp) ptx::mma_ts_elect(d_o, a_p + ks * 8, bd, idPV, 1u);
+            else ptx::mma_ts(d_o, a_p + ks * 8, bd, idPV, 1u);
+          }
+#pragma unroll
+          for (int ks = 0; ks < Dh / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            const uint64_t ad = ptx::smem_desc_sw128(a_addr + t * (Dh * 256) + off, 16, 1024);
+            const uint64_t bd = ptx::smem_desc_sw128(b_addr + off, 16, 1024);
+            if constexpr (kWarp) ptx::mma_ss_elect(tmem + 128 * t, ad, bd, idS, ks > 0);
+            else ptx::mma_ss(tmem + 128 * t, ad, bd, idS, ks > 0);
+          }
+          if constexpr (kWarp) ptx::mma_commit_elect(&sink);
+          else ptx::mma_commit(&sink);
+        }
+      }
+      if constexpr (kWarp) ptx::mma_commit_elect(&done);
+      else ptx::mma_commit(&done);
+      if (threadIdx.x == 0) {
+        volatile int dummy_abort = 0;
+        int dummy_status = 0;
+        (void)ptx::mbar_wait(&done, 0, &dummy_abort, &dummy_status, 2000000000ull);
       }
     }
   } else if (threadIdx.x == 0) {
@@ -208,6 +251,12 @@ attn_status launch_mma_probe(int n, int mode, int iters, cudaStream_t stream) {
     e = launch_probe<128, 6>(iters, grid, stream);
   else if (mode == 7)
     e = launch_probe<128, 7>(iters, grid, stream);
+  else if (mode == 8)
+    e = launch_probe<128, 8>(iters, grid, stream);
+  else if (mode == 9)
+    e = launch_probe<128, 9>(iters, grid, stream);
+  else if (mode == 10)
+    e = launch_probe<128, 10>(iters, grid, stream);
   else if (n == 64)
     e = mode ? launch_probe<64, 1>(iters, grid, stream) : launch_probe<64, 0>(iters, grid, stream);
   else if (n == 128)

@@ -176,8 +176,13 @@ CPATTN_API int attn_set_max_ctas(int n);
  *   round trips of one 128x128x128 GEMM -> commit -> a second warp waits, reads tensor memory
  *   and arrives -> the issuing thread waits (hand-off latency); modes 5 / 6 / 7 (n = 128): mode
  *   2 while four other warps stream tensor-memory loads and stores / run dependent FMA chains /
- *   run independent FMA chains (contention).  The caller times the launch:
- *   flops = SMs * iters * 2*128*n*16.  ATTN_ERR_INVALID_ARG for other arguments.
+ *   run independent FMA chains (contention); mode 8 (n = 128): the D = 64 per-step sequence
+ *   (per query tile 8 A-from-tensor-memory MMAs with N = 64, then 4 shared-memory MMAs with
+ *   N = 128, one commit; two tiles) issued by a single lane, iters/24 steps; mode 9: the same
+ *   issued by a converged warp through elect.sync; mode 10: the D = 128 sequence of mode 2
+ *   issued through elect.sync, iters/32 steps.  The caller times the launch:
+ *   flops = SMs * iters * 2*128*n*16 for modes 0-7, SMs * steps * 2 * 4*128*128*D for 8-10.
+ *   ATTN_ERR_INVALID_ARG for other arguments.
  */
 CPATTN_API attn_status attn_probe_mma(int n, int mode, int iters, attn_stream_t stream);
 

@@ -162,3 +162,13 @@ def test_ulysses_argument_errors(L_):
     assert uly(L_, lse=O + 64) == E                 # lse inside o
     assert uly(L_, B=0) == cpattn.ATTN_OK           # empty problems touch nothing
     assert uly(L_, S=0) == cpattn.ATTN_OK
+
+
+def test_probe_argument_errors(L_):
+    E = cpattn.ATTN_ERR_INVALID_ARG
+    f = L_.attn_probe_mma
+    assert f(96, 0, 100, None) == E       # N must be 64, 128 or 256
+    assert f(128, 11, 100, None) == E     # unknown mode
+    assert f(128, -1, 100, None) == E
+    assert f(64, 2, 100, None) == E       # the step sequences need n = 128
+    assert f(128, 0, 0, None) == E        # no iterations
