@@ -73,10 +73,14 @@ struct Cfg {
   static constexpr int NH = D / 64;                       // 64-wide halves per row
   static constexpr int TILE = NH * kHalfBytes;            // bytes of one 128-row tile
   static constexpr int STAGES = (D == 128) ? 5 : 8;       // K/V ring depth
-  static constexpr int NBARS = 2 * STAGES + 8 * kQT + 1;
+  static constexpr int NBARS = 2 * STAGES + 10 * kQT + 2;
   static constexpr int SMEM = 1024 /*alignment slack*/ + kQT * TILE + STAGES * TILE +
                               NBARS * 8 + 16;
   static constexpr uint32_t S_COL0 = 0, S_COL1 = 128, O_COL0 = 256, O_COL1 = 256 + D;
+  // D = 64 leaves 128 columns free: P gets its own columns, so S(j+1) can be computed while the
+  // softmax of S(j) runs (separate-P schedule).  D = 128 writes P over the first half of S.
+  static constexpr bool SEP_P = (D == 64);
+  static constexpr uint32_t P_COL0 = SEP_P ? 384 : S_COL0, P_COL1 = SEP_P ? 448 : S_COL1;
 };
 
 struct Params {
@@ -183,15 +187,17 @@ struct NoHook {
 };
 
 // One KV tile of the online softmax for this thread's row: read the 128 logits from TMEM at
-// s_addr (then run after_load: the logits are in registers), update the running max m (only
+// s_addr (then run after_load: the logits are in registers; before_store runs before the first
+// write to p_addr), update the running max m (only
 // when it grows by more than the threshold; `need` reports a move and `alpha` = 2^(m_old -
 // m_new), or 1), write P = 2^(s*scale*log2(e) - m) as 16-bit pairs to the 64 TMEM columns at
 // p_addr, and return the row sum of P.  kMasked treats columns >= valid as -inf (last tile of a
 // KV chunk).
-template <bool BF16, bool kMasked, typename AfterLoad = NoHook>
+template <bool BF16, bool kMasked, typename AfterLoad = NoHook, typename BeforeStore = NoHook>
 __device__ __forceinline__ float softmax_tile(uint32_t s_addr, uint32_t p_addr, float sl2,
                                               int valid, float& m, bool& need, float& alpha,
-                                              AfterLoad after_load = AfterLoad()) {
+                                              AfterLoad after_load = AfterLoad(),
+                                              BeforeStore before_store = BeforeStore()) {
   uint32_t sr[kBN];
   ptx::tmem_ld128(s_addr, sr);
   after_load();
@@ -234,6 +240,7 @@ __device__ __forceinline__ float softmax_tile(uint32_t s_addr, uint32_t p_addr, 
       lacc[c & 3] = ptx::f2_add(lacc[c & 3], ptx::f2_pack(p0, p1));
       pk[c] = ptx::pack2<BF16>(p0, p1);
     }
+    if (h == 0) before_store();
     ptx::tmem_st16(p_addr + 16 * h, pk);
   }
 #undef SV
@@ -290,7 +297,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = s_full + kQT;
   uint64_t* o_full = p_full + kQT;
   uint64_t* o_empty = o_full + kQT;
-  uint64_t* mma_drain = o_empty + kQT;
+  uint64_t* s_free = o_empty + kQT;     // separate-P schedule: S tile read into registers
+  uint64_t* pv_done = s_free + kQT;     // separate-P schedule: P*V of the tile completed
+  uint64_t* mma_drain = pv_done + kQT;   // [0]: MMA warp, [1]: P*V warp (separate-P schedule)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -310,8 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&p_full[t], 4);
       ptx::mbar_init(&o_full[t], 1);
       ptx::mbar_init(&o_empty[t], 4);
+      ptx::mbar_init(&s_free[t], 4);
+      ptx::mbar_init(&pv_done[t], 1);
     }
-    ptx::mbar_init(mma_drain, 1);
+    ptx::mbar_init(&mma_drain[0], 1);
+    ptx::mbar_init(&mma_drain[1], 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -374,10 +386,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (q_issued[t] >= 0) drain_wait(&q_full[t], q_issued[t] & 1, lim);
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------------ MMA issuer
-    // The whole warp runs this loop with identical control flow (every wait is voted across
-    // the warp); one elected lane issues each MMA and commit.
+  } else if (warp == kMmaWarp || (C::SEP_P && warp == kMmaWarp + 1)) {
+    // ------------------------------------------------------------------ MMA issuers
+    // The whole warp runs its loop with identical control flow (every wait is voted across
+    // the warp); one elected lane issues each MMA and commit.  With separate P the S = Q K^T
+    // GEMMs (this warp) and the O += P V GEMMs (the next warp) touch disjoint tensor-memory
+    // columns and are ordered only through the softmax hand-offs, so two warps issue them:
+    // each issuing warp is a serial chain of waits and issues, and splitting it halves the
+    // chain per KV step.
     {
       constexpr uint32_t kIdescS = ptx::idesc_f16(BF16, false, kBM, kBN);
       constexpr uint32_t kIdescPV = ptx::idesc_f16(BF16, true, kBM, D);
@@ -398,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv = [&](int t, uint32_t st, bool acc) {
         const uint32_t b0 = sKV_addr + st * C::TILE;
         const uint32_t d_o = tmem + (t == 0 ? C::O_COL0 : C::O_COL1);
-        const uint32_t a_p = tmem + (t == 0 ? C::S_COL0 : C::S_COL1);
+        const uint32_t a_p = tmem + (t == 0 ? C::P_COL0 : C::P_COL1);
 #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks) {
           ptx::mma_ts_elect(d_o, a_p + ks * 8,
@@ -417,6 +433,60 @@ __global__ void __launch_bounds__(kThreads, 1)
                           ptx::mbar_wait(&kv_full[st], ph, abort_flag, &g_attn_status, lim));
       };
 
+      uint32_t sfph[2] = {0, 0};
+      auto vote_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu,
+                          ptx::mbar_wait(bar, parity, abort_flag, &g_attn_status, lim));
+      };
+      if constexpr (C::SEP_P) {
+        // The loader fills ring positions K_0, V_0, K_1, V_1, ...; with an even number of
+        // stages the K tiles always land in even stages (consumed here by the S warp) and the
+        // V tiles in odd ones (the P*V warp), so each stage has one consumer.
+        static_assert(C::STAGES % 2 == 0, "K and V stages must alternate");
+        const bool s_role = warp == kMmaWarp;
+        uint32_t pos = s_role ? 0u : 1u;   // ring position of this warp's next tile
+        auto wait_tile = [&](uint32_t& st) -> bool {
+          st = pos % C::STAGES;
+          const uint32_t ph = (pos / C::STAGES) & 1;
+          pos += 2;
+          return vote_wait(&kv_full[st], ph);
+        };
+        for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
+          const Unit w = decode_unit(u, p);
+          for (int j = 0; ok && j < w.n; ++j) {
+            uint32_t st;
+            if (!(ok = wait_tile(st))) break;
+            for (int t = 0; t < kQT; ++t) {
+              if (s_role) {
+                // S_t(j) overwrites the S columns of S_t(j-1) (or of the previous unit's last
+                // tile): wait until the softmax has them in registers.
+                if (j > 0 || it > 0) {
+                  if (!(ok = vote_wait(&s_free[t], sfph[t]))) break;
+                  sfph[t] ^= 1;
+                }
+                if (j == 0 && !(ok = vote_wait(&q_full[t], it & 1))) break;
+                ptx::tc_fence_after();
+                issue_s(t, st);
+                ptx::mma_commit_elect(&s_full[t]);
+                if (j == w.n - 1) ptx::mma_commit_elect(&q_empty[t]);
+              } else {
+                if (!(ok = vote_wait(&p_full[t], pph[t]))) break;
+                pph[t] ^= 1;
+                if (j == 0 && it > 0 && !(ok = vote_wait(&o_empty[t], (it - 1) & 1))) break;
+                ptx::tc_fence_after();
+                issue_pv(t, st, j > 0);
+                ptx::mma_commit_elect(&pv_done[t]);
+                if (j == w.n - 1) ptx::mma_commit_elect(&o_full[t]);
+              }
+            }
+            if (!ok) break;
+            ptx::mma_commit_elect(&kv_empty[st]);
+          }
+        }
+        // All MMAs this warp issued complete before TMEM is released.
+        ptx::mma_commit_elect(&mma_drain[s_role ? 0 : 1]);
+        drain_wait(&mma_drain[s_role ? 0 : 1], 0, lim);
+      } else {
       for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
         const Unit w = decode_unit(u, p);
         uint32_t sk, sv;
@@ -462,8 +532,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // All MMAs this warp issued complete before TMEM is released.
-      ptx::mma_commit_elect(mma_drain);
-      drain_wait(mma_drain, 0, lim);
+      ptx::mma_commit_elect(&mma_drain[0]);
+      drain_wait(&mma_drain[0], 0, lim);
+      }
     }
   }
   } else {
@@ -475,9 +546,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t s_addr = tmem + lane_base + (t == 0 ? C::S_COL0 : C::S_COL1);
     const uint32_t o_addr = tmem + lane_base + (t == 0 ? C::O_COL0 : C::O_COL1);
+    const uint32_t p_addr = tmem + lane_base + (t == 0 ? C::P_COL0 : C::P_COL1);
     const float sl2 = p.scale_log2;
-    uint32_t sph = 0, oph = 0, it = 0;
+    uint32_t sph = 0, oph = 0, it = 0, pdph = 0;
     bool ok = true;
+    bool pv_pending = false;   // separate-P schedule: a P*V of this tile may still read P
+
+    // Separate-P schedule hooks (no-ops when P overwrites S): release the S columns as soon as
+    // the logits are in registers; before overwriting P, wait for the P*V that reads it.
+    auto after_load = [&]() {
+      if constexpr (C::SEP_P) {
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&s_free[t]);
+      }
+    };
+    auto before_store = [&]() {
+      if constexpr (C::SEP_P) {
+        if (pv_pending) {
+          ok = __all_sync(0xffffffffu,
+                          ptx::mbar_wait(&pv_done[t], pdph, abort_flag, &g_attn_status, lim));
+          pdph ^= 1;
+          ptx::tc_fence_after();
+        }
+        pv_pending = true;
+      }
+    };
 
     for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
       const Unit w = decode_unit(u, p);
@@ -494,12 +588,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         float alpha;
         const float l_tile =
             (j == w.n - 1 && w.last_valid < kBN)
-                ? softmax_tile<BF16, true>(s_addr, s_addr, sl2, w.last_valid, m, need, alpha)
-                : softmax_tile<BF16, false>(s_addr, s_addr, sl2, kBN, m, need, alpha);
+                ? softmax_tile<BF16, true>(s_addr, p_addr, sl2, w.last_valid, m, need, alpha,
+                                           after_load, before_store)
+                : softmax_tile<BF16, false>(s_addr, p_addr, sl2, kBN, m, need, alpha, after_load,
+                                            before_store);
+        if (!ok) break;
         l = l * alpha + l_tile;
-        // Rescale O (the P*V of earlier steps, whose MMAs completed before S_j was signalled)
-        // when the max moved in any row of this warp.  P*V of this step is only issued after
-        // the arrive below, so O is not in use.
+        // Rescale O when the max moved in any row of this warp.  O is not in use: the P*V of
+        // earlier steps completed before S_j was signalled (P over S), or before pv_done was
+        // observed above (separate P); this step's P*V is only issued after the arrive below.
         if (j > 0 && __any_sync(0xffffffffu, need)) rescale_o<D>(o_addr, alpha);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();

@@ -136,8 +136,7 @@ __global__ void __launch_bounds__(256, 1) mma_probe_kernel(int iters) {
       else ptx::mma_commit(&done);
       if (threadIdx.x == 0) {
         volatile int dummy_abort = 0;
-        int dummy_status = 0;
-        (void)ptx::mbar_wait(&done, 0, &dummy_abort, &dummy_status, 2000000000ull);
+        (void)ptx::mbar_wait(&done, 0, &dummy_abort, &g_probe_status, 2000000000ull);
       }
     }
   } else if (threadIdx.x == 0) {
@@ -177,8 +176,7 @@ __global__ void __launch_bounds__(256, 1) mma_probe_kernel(int iters) {
     }
     ptx::mma_commit(&done);
     volatile int dummy_abort = 0;
-    int dummy_status = 0;
-    (void)ptx::mbar_wait(&done, 0, &dummy_abort, &dummy_status, 2000000000ull);
+    (void)ptx::mbar_wait(&done, 0, &dummy_abort, &g_probe_status, 2000000000ull);
     stop_flag = 1;
   } else if (kMode >= 5 && threadIdx.x >= 128) {
     // background load on warps 4-7 (TMEM lane quarter = warp % 4) until the MMAs are done
