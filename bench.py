@@ -251,6 +251,7 @@ def run_native(args, rank, world, local_rank):
     }
     legs.update(_layout_leg(cpattn, dev, stream, peaks))
     legs.update(_ulysses_leg(cpattn, dev, stream))
+    legs.update(_ring_leg(cpattn, qd, kd, vd, o, lse, dev, stream, flops, ms_per_step))
     clk = clocks.summary()
 
     e2e = None
@@ -441,6 +442,26 @@ def run_reference(args):
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
+
+
+def _ring_leg(cpattn, qd, kd, vd, o, lse, dev, stream, flops, step_ms, iters=5):
+    """The same video problem through attn_fwd_ring (P = 8 ring steps, merge fused into the
+    kernel: no partial outputs in HBM, no merge launch), against the step above."""
+    cpattn.attn_fwd_ring(qd, kd, vd, P_CHUNKS, o, lse, stream=stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(iters)]
+    for a, b in evs:
+        a.record(stream)
+        cpattn.attn_fwd_ring(qd, kd, vd, P_CHUNKS, o, lse, stream=stream)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    st = cpattn.attn_device_status(stream)
+    if st != cpattn.ATTN_OK:
+        raise RuntimeError(f"device status after ring leg: {cpattn.attn_status_string(st)}")
+    ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+    return {"attn_fwd_ring_P8": {"median_ms": round(ms, 4),
+                                 "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1),
+                                 "vs_chunked_plus_merge_step_ms": round(step_ms, 4)}}
 
 
 def _ulysses_leg(cpattn, dev, stream, iters=5):

@@ -14,7 +14,8 @@ from typing import Optional, Tuple
 import torch
 
 __all__ = ["CpAttnError", "CpAttnLibraryError", "lib", "attn_fwd", "attn_fwd_chunked",
-           "attn_lse_merge", "attn_fwd_ulysses", "cp_layout_seq2head", "cp_layout_head2seq", "attn_device_status",
+           "attn_lse_merge", "attn_fwd_ulysses", "attn_fwd_ring", "cp_layout_seq2head",
+           "cp_layout_head2seq", "attn_device_status",
            "attn_watchdog_selftest", "attn_set_max_ctas", "attn_probe_mma",
            "attn_set_kernel_variant", "attn_status_string", "attn_version",
            "LIB_PATH", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
@@ -59,6 +60,7 @@ def lib() -> ctypes.CDLL:
     L.attn_fwd_chunked.argtypes = [vp, vp, vp, i, vp, fp, i, i, i, i, i, i, f, vp]
     L.attn_lse_merge.argtypes = [vp, fp, i, i, i, i, i, i, vp, fp, vp]
     L.attn_fwd_ulysses.argtypes = [vp, vp, vp, vp, fp, i, i, i, i, i, i, f, vp]
+    L.attn_fwd_ring.argtypes = [vp, vp, vp, i, vp, fp, i, i, i, i, i, i, f, vp]
     L.cp_layout_seq2head.argtypes = [vp, vp, i, i, i, i, i, i, vp]
     L.cp_layout_head2seq.argtypes = [vp, vp, i, i, i, i, i, i, vp]
     L.attn_status_string.argtypes = [i]
@@ -70,10 +72,9 @@ def lib() -> ctypes.CDLL:
     L.attn_probe_mma.argtypes = [i, i, i, vp]
     L.attn_version.argtypes = []
     for name in ("attn_fwd", "attn_fwd_chunked", "attn_lse_merge", "attn_fwd_ulysses",
-                 "cp_layout_seq2head",
-                 "cp_layout_head2seq", "attn_device_status", "attn_watchdog_selftest",
-                 "attn_set_max_ctas", "attn_version", "attn_probe_mma",
-                 "attn_set_kernel_variant"):
+                 "attn_fwd_ring", "cp_layout_seq2head", "cp_layout_head2seq",
+                 "attn_device_status", "attn_watchdog_selftest", "attn_set_max_ctas",
+                 "attn_version", "attn_probe_mma", "attn_set_kernel_variant"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -165,6 +166,22 @@ def attn_lse_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor,
     _check("attn_lse_merge", lib().attn_lse_merge(
         _dev(o_parts, "o_parts"), _dev(lse_parts, "lse_parts"), P, B, H, Sq, D,
         _DT[o_parts.dtype], _dev(o, "o"), _ptr_or_null(lse, "lse"), _stream(stream)))
+    return o, lse
+
+
+def attn_fwd_ring(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int,
+                  o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                  scale: float = 0.0, want_lse: bool = True, stream=None):
+    """Ring attention over P KV chunks with the merge fused in: O [B,H,Sq,D], LSE [B,H,Sq]."""
+    B, H, Sq, D = q.shape
+    Skv = k.shape[2]
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    _check("attn_fwd_ring", lib().attn_fwd_ring(
+        _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), P, _dev(o, "o"), _ptr_or_null(lse, "lse"),
+        B, H, Sq, Skv, D, _DT[q.dtype], float(scale), _stream(stream)))
     return o, lse
 
 

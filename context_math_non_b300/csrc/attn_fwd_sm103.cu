@@ -141,11 +141,60 @@ struct Unit {
   int qb, c, bh, lo, n, last_valid;
 };
 
+// Ring mode: the KV tiles of a unit, chunk by chunk in ring order.  Chunk c (the KV block rank c
+// holds) is cut into 128-row tiles starting at its first row, the last tile masked at the chunk
+// end; after the last tile of chunk c comes chunk c - 1 (mod P), as a rank receives its
+// neighbour's block at each ring step.
+struct KvCursor {
+  int c, left, tile, nt, lo, last_valid;
+};
+
 // Chunk c covers KV rows [floor(c*Skv/P), floor((c+1)*Skv/P)); with Skv = q*P + r,
 // floor(c*Skv/P) = c*q + floor(c*r/P), and c*r < P^2 <= 2^32 fits 32-bit unsigned arithmetic.
 __device__ __forceinline__ int chunk_start(int c, const Params& p) {
   return c * p.kv_q + static_cast<int>((static_cast<uint32_t>(c) * static_cast<uint32_t>(p.kv_r)) /
                                        static_cast<uint32_t>(p.P));
+}
+
+__device__ __forceinline__ void cursor_load(KvCursor& k, const Params& p) {
+  k.lo = chunk_start(k.c, p);
+  const int len = chunk_start(k.c + 1, p) - k.lo;
+  k.nt = (len + kBN - 1) / kBN;
+  k.last_valid = len - (k.nt - 1) * kBN;
+  k.tile = 0;
+}
+__device__ __forceinline__ void cursor_start(KvCursor& k, const Unit& w, const Params& p) {
+  k.c = w.c;
+  k.left = p.P;
+  cursor_load(k, p);
+}
+__device__ __forceinline__ int cursor_row(const KvCursor& k) { return k.lo + k.tile * kBN; }
+__device__ __forceinline__ int cursor_valid(const KvCursor& k) {
+  return k.tile == k.nt - 1 ? k.last_valid : kBN;
+}
+__device__ __forceinline__ void cursor_next(KvCursor& k, const Params& p) {
+  if (++k.tile == k.nt && --k.left > 0) {
+    k.c = (k.c == 0 ? p.P : k.c) - 1;
+    cursor_load(k, p);
+  }
+}
+
+// Ring mode unit u = (bh, qb): all P chunks.  The block starts at the chunk of the rank that
+// holds its first query row (queries split into P ranks like the keys), and the tile count is
+// the sum over chunks: with Skv = q*P + r, r chunks have q + 1 rows and P - r have q.
+__device__ __forceinline__ Unit decode_ring_unit(int u, const Params& p) {
+  Unit w;
+  const uint32_t uu = static_cast<uint32_t>(u);
+  const uint32_t bh = uu / static_cast<uint32_t>(p.n_qb);
+  w.qb = static_cast<int>(uu - bh * static_cast<uint32_t>(p.n_qb));
+  w.bh = static_cast<int>(bh);
+  const long long row0 = static_cast<long long>(w.qb) * (kQT * kBM);
+  const long long c0 = ((row0 + 1) * p.P - 1) / p.Sq;
+  w.c = static_cast<int>(c0 < p.P - 1 ? c0 : p.P - 1);
+  w.lo = 0;
+  w.n = (p.P - p.kv_r) * ((p.kv_q + kBN - 1) / kBN) + p.kv_r * ((p.kv_q + kBN) / kBN);
+  w.last_valid = kBN;
+  return w;
 }
 
 __device__ __forceinline__ Unit decode_unit(int u, const Params& p) {
@@ -277,7 +326,7 @@ __device__ __forceinline__ void rescale_o(uint32_t o_addr, float alpha) {
   }
 }
 
-template <int D, bool BF16, bool kSeq>
+template <int D, bool BF16, bool kSeq, bool kRing>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -352,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < kQT; ++t) q_issued[t] = -1;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
-        const Unit w = decode_unit(u, p);
+        const Unit w = kRing ? decode_ring_unit(u, p) : decode_unit(u, p);
         for (int t = 0; ok && t < kQT; ++t) {
           ok = ptx::mbar_wait(&q_empty[t], (it & 1) ^ 1, abort_flag, &g_attn_status, lim);
           if (!ok) break;
@@ -362,7 +411,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             load_rows<kSeq>(sQ + t * C::TILE + h * kHalfBytes, &tm_q, 64 * h,
                             w.qb * (kQT * kBM) + t * kBM, w.bh, &q_full[t], p);
         }
+        KvCursor kc;
+        if constexpr (kRing) cursor_start(kc, w, p);
         for (int j = 0; ok && j < w.n; ++j) {
+          const int kv_row = kRing ? cursor_row(kc) : w.lo + j * kBN;
+          if constexpr (kRing) cursor_next(kc, p);
           for (int which = 0; which < 2; ++which) {
             const uint32_t st = kv_pos % C::STAGES;
             const uint32_t ph = (kv_pos / C::STAGES) & 1;
@@ -371,8 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_arrive_expect_tx(&kv_full[st], C::TILE);
             const CUtensorMap* map = which == 0 ? &tm_k : &tm_v;
             for (int h = 0; h < C::NH; ++h)
-              load_rows<kSeq>(sKV + st * C::TILE + h * kHalfBytes, map, 64 * h,
-                              w.lo + j * kBN, w.bh, &kv_full[st], p);
+              load_rows<kSeq>(sKV + st * C::TILE + h * kHalfBytes, map, 64 * h, kv_row, w.bh,
+                              &kv_full[st], p);
             ++kv_pos;
           }
         }
@@ -404,21 +457,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a0 = sQ_addr + t * C::TILE;
         const uint32_t b0 = sKV_addr + st * C::TILE;
         const uint32_t d_s = tmem + (t == 0 ? C::S_COL0 : C::S_COL1);
+        const uint64_t da = ptx::smem_desc_sw128(a0, 16, 1024);
+        const uint64_t db = ptx::smem_desc_sw128(b0, 16, 1024);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-          ptx::mma_ss_elect(d_s, ptx::smem_desc_sw128(a0 + off, 16, 1024),
-                            ptx::smem_desc_sw128(b0 + off, 16, 1024), kIdescS, ks > 0);
+          // descriptor start-address field counts 16-byte units; no carry can leave it
+          const uint64_t off = static_cast<uint64_t>(((ks >> 2) * kHalfBytes + (ks & 3) * 32) >> 4);
+          ptx::mma_ss_elect(d_s, da + off, db + off, kIdescS, ks > 0);
         }
       };
       auto issue_pv = [&](int t, uint32_t st, bool acc) {
         const uint32_t b0 = sKV_addr + st * C::TILE;
         const uint32_t d_o = tmem + (t == 0 ? C::O_COL0 : C::O_COL1);
         const uint32_t a_p = tmem + (t == 0 ? C::P_COL0 : C::P_COL1);
+        const uint64_t dv = ptx::smem_desc_sw128(b0, kHalfBytes, 1024);
 #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks) {
-          ptx::mma_ts_elect(d_o, a_p + ks * 8,
-                            ptx::smem_desc_sw128(b0 + ks * 2048, kHalfBytes, 1024), kIdescPV,
+          ptx::mma_ts_elect(d_o, a_p + ks * 8, dv + static_cast<uint64_t>(ks * 128), kIdescPV,
                             (acc || ks > 0) ? 1u : 0u);
         }
       };
@@ -452,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           return vote_wait(&kv_full[st], ph);
         };
         for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
-          const Unit w = decode_unit(u, p);
+          const Unit w = kRing ? decode_ring_unit(u, p) : decode_unit(u, p);
           for (int j = 0; ok && j < w.n; ++j) {
             uint32_t st;
             if (!(ok = wait_tile(st))) break;
@@ -488,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         drain_wait(&mma_drain[s_role ? 0 : 1], 0, lim);
       } else {
       for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
-        const Unit w = decode_unit(u, p);
+        const Unit w = kRing ? decode_ring_unit(u, p) : decode_unit(u, p);
         uint32_t sk, sv;
         if (!(ok = wait_kv(sk))) break;
         for (int t = 0; t < kQT; ++t) {
@@ -574,9 +629,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
-      const Unit w = decode_unit(u, p);
+      const Unit w = kRing ? decode_ring_unit(u, p) : decode_unit(u, p);
       float m = -INFINITY;   // running max of scaled logits, log2 units
       float l = 0.f;         // running denominator relative to m
+      KvCursor kc;
+      if constexpr (kRing) cursor_start(kc, w, p);
       for (int j = 0; j < w.n; ++j) {
         ok = __all_sync(0xffffffffu,
                         ptx::mbar_wait(&s_full[t], sph, abort_flag, &g_attn_status, lim));
@@ -586,9 +643,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         bool need;
         float alpha;
+        int valid;
+        if constexpr (kRing) {
+          valid = cursor_valid(kc);
+          cursor_next(kc, p);
+        } else {
+          valid = j == w.n - 1 ? w.last_valid : kBN;
+        }
         const float l_tile =
-            (j == w.n - 1 && w.last_valid < kBN)
-                ? softmax_tile<BF16, true>(s_addr, p_addr, sl2, w.last_valid, m, need, alpha,
+            valid < kBN
+                ? softmax_tile<BF16, true>(s_addr, p_addr, sl2, valid, m, need, alpha,
                                            after_load, before_store)
                 : softmax_tile<BF16, false>(s_addr, p_addr, sl2, kBN, m, need, alpha, after_load,
                                             before_store);
@@ -614,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q_row = w.qb * (kQT * kBM) + t * kBM + row;
       const bool valid = q_row < p.Sq;
       const float inv_l = 1.f / l;
-      const long long prow = static_cast<long long>(w.c) * p.BH + w.bh;
+      const long long prow = static_cast<long long>(kRing ? 0 : w.c) * p.BH + w.bh;
       uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
                        out_row_offset<kSeq, D>(prow, w.bh, valid ? q_row : 0, p);
 #pragma unroll
@@ -1058,10 +1122,10 @@ cudaError_t launch_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
   return cudaGetLastError();
 }
 
-template <int D, bool BF16, bool kSeq = false>
+template <int D, bool BF16, bool kSeq = false, bool kRing = false>
 cudaError_t launch_typed(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const Params& p, int grid, cudaStream_t stream) {
-  auto kern = attn_fwd_kernel<D, BF16, kSeq>;
+  auto kern = attn_fwd_kernel<D, BF16, kSeq, kRing>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int regs = -1;
@@ -1096,13 +1160,14 @@ int set_attention_variant(int v) { return g_variant.exchange(v); }
 
 attn_status launch_attention(const void* q, const void* k, const void* v, void* o, float* lse,
                              int P, int B, int H, int Sq, int Skv, int D, bool bf16, float scale,
-                             cudaStream_t stream, unsigned long long limit_ns, int max_ctas) {
+                             cudaStream_t stream, unsigned long long limit_ns, int max_ctas,
+                             bool ring) {
   const int BH = B * H;
   int sms = device_sm_count();
   if (sms <= 0) return ATTN_ERR_CUDA;
   if (max_ctas > 0 && max_ctas < sms) sms = max_ctas;
   // D = 128 runs on CTA pairs (needs at least one pair of SMs); D = 64 on single CTAs.
-  const bool pair = D == 128 && g_variant.load() == 1 && sms >= 2;
+  const bool pair = !ring && D == 128 && g_variant.load() == 1 && sms >= 2;
   const int rows_per_unit = pair ? 4 * kBM : kQT * kBM;
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, bf16, D, Sq, BH) || !make_map(&mk, k, bf16, D, Skv, BH, pair ? 64 : 128) ||
@@ -1114,7 +1179,7 @@ attn_status launch_attention(const void* q, const void* k, const void* v, void* 
   p.P = P;
   p.BH = BH;
   p.n_qb = (Sq + rows_per_unit - 1) / rows_per_unit;
-  const long long units = static_cast<long long>(BH) * P * p.n_qb;
+  const long long units = static_cast<long long>(BH) * (ring ? 1 : P) * p.n_qb;
   if (units >= (1ll << 31) || P > 65536) return ATTN_ERR_UNSUPPORTED;
   p.num_units = static_cast<int>(units);
   p.kv_q = Skv / P;
@@ -1130,12 +1195,20 @@ attn_status launch_attention(const void* q, const void* k, const void* v, void* 
              : launch_pair<false>(mq, mk, mv, p, 2 * pairs, stream);
   } else {
     const int grid = p.num_units < sms ? p.num_units : sms;
-    if (D == 128)
+    if (ring) {
+      if (D == 128)
+        e = bf16 ? launch_typed<128, true, false, true>(mq, mk, mv, p, grid, stream)
+                 : launch_typed<128, false, false, true>(mq, mk, mv, p, grid, stream);
+      else
+        e = bf16 ? launch_typed<64, true, false, true>(mq, mk, mv, p, grid, stream)
+                 : launch_typed<64, false, false, true>(mq, mk, mv, p, grid, stream);
+    } else if (D == 128) {
       e = bf16 ? launch_typed<128, true>(mq, mk, mv, p, grid, stream)
                : launch_typed<128, false>(mq, mk, mv, p, grid, stream);
-    else
+    } else {
       e = bf16 ? launch_typed<64, true>(mq, mk, mv, p, grid, stream)
                : launch_typed<64, false>(mq, mk, mv, p, grid, stream);
+    }
   }
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

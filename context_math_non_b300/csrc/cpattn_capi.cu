@@ -105,6 +105,20 @@ attn_status attn_fwd_chunked(const void* q, const void* k, const void* v, int P,
                                   cpattn::kDefaultWaitLimitNs, g_max_ctas.load());
 }
 
+attn_status attn_fwd_ring(const void* q, const void* k, const void* v, int P, void* o, float* lse,
+                          int B, int H, int Sq, int Skv, int D, attn_dtype dt, float scale,
+                          attn_stream_t stream) {
+  bool empty;
+  // O and LSE are single outputs here: validate them as the P = 1 problem, then check P alone.
+  attn_status st = check_attention(q, k, v, o, lse, 1, B, H, Sq, Skv, D, dt, &empty);
+  if (st != ATTN_OK) return st;
+  if (P < 1 || P > Skv) return ATTN_ERR_INVALID_ARG;
+  if (empty) return ATTN_OK;
+  return cpattn::launch_attention(q, k, v, o, lse, P, B, H, Sq, Skv, D, dt == ATTN_BF16,
+                                  resolve_scale(scale, D), reinterpret_cast<cudaStream_t>(stream),
+                                  cpattn::kDefaultWaitLimitNs, g_max_ctas.load(), true);
+}
+
 attn_status attn_fwd_ulysses(const void* q, const void* k, const void* v, void* o, float* lse,
                              int P, int B, int S, int H, int D, attn_dtype dt, float scale,
                              attn_stream_t stream) {

@@ -13,10 +13,13 @@ constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
 int device_sm_count();
 
 // Attention over P KV chunks (P = 1: plain attention).  Arguments already validated.
-// max_ctas > 0 caps the persistent grid (testing only); 0 = one CTA per SM.
+// max_ctas > 0 caps the persistent grid (testing only); 0 = one CTA per SM.  ring = false: one
+// partial (O_c, LSE_c) per chunk; ring = true: every query block walks all P chunks in ring
+// order keeping its running softmax state on chip, and writes one merged O and LSE.
 attn_status launch_attention(const void* q, const void* k, const void* v, void* o, float* lse,
                              int P, int B, int H, int Sq, int Skv, int D, bool bf16, float scale,
-                             cudaStream_t stream, unsigned long long limit_ns, int max_ctas);
+                             cudaStream_t stream, unsigned long long limit_ns, int max_ctas,
+                             bool ring = false);
 
 // 1: D = 128 attention runs on CTA pairs; 0 (default): single-CTA kernel for every D.
 // Returns the previous setting.

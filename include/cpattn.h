@@ -120,6 +120,25 @@ CPATTN_API attn_status cp_layout_head2seq(const void* in, void* out, int P, int 
                                int elem_bytes, attn_stream_t stream);
 
 /*
+ * attn_fwd_ring -- Ring Attention with the merge fused into the attention kernel.
+ *   Defines: page section "Ring Attention" (Figure 3) -- each rank keeps its query block, the
+ *   KV blocks travel around the ring, and after every step the rank updates its attention
+ *   output with the block it just received.  Here rank c's KV block is chunk c of K/V (chunk
+ *   bounds as in attn_fwd_chunked) and the query rows are split into P ranks the same way; each
+ *   block of 256 query rows starts at the chunk of the rank that holds its first row and then
+ *   takes the chunks c-1, c-2, ... (mod P), every chunk cut into 128-row tiles from its own first
+ *   row (last tile masked at the chunk end).  The running max, denominator and output stay on
+ *   chip across chunks, so no partial output reaches memory and no merge pass runs.  Result:
+ *   full attention over Skv keys, equal to attn_lse_merge(attn_fwd_chunked(P)) and to attn_fwd
+ *   up to fp32 summation order.
+ *   q [B][H][Sq][D], k, v [B][H][Skv][D] dtype `dt`; o [B][H][Sq][D]; lse [B][H][Sq] fp32 or NULL.
+ *   1 <= P <= Skv (ATTN_ERR_INVALID_ARG otherwise); other requirements as attn_fwd.
+ */
+CPATTN_API attn_status attn_fwd_ring(const void* q, const void* k, const void* v, int P, void* o,
+                                     float* lse, int B, int H, int Sq, int Skv, int D,
+                                     attn_dtype dt, float scale, attn_stream_t stream);
+
+/*
  * attn_fwd_ulysses -- DeepSpeed Ulysses attention without the two re-layout passes.
  *   Defines: page subsection "DeepSpeed Ulysses" and Figure 4 -- after the first all-to-all each
  *   rank attends over the full sequence for its subset of heads, and the second all-to-all

@@ -3,8 +3,10 @@
 TEST INFRASTRUCTURE ONLY: imported by the tests, ``__graft_entry__.smoke()`` and the CPU-baseline
 legs of ``bench.py``; never by the product library or its Python binding.
 """
-from .cp_attention import (attention, attention_chunked, attention_online, chunk_bounds, head2seq,
-                        lse_merge, seq2head, softmax_weights, to_f64, ulysses_attention)
+from .cp_attention import (attention, attention_chunked, attention_online, attention_ring,
+                           chunk_bounds, head2seq, lse_merge, seq2head, softmax_weights, to_f64,
+                           ulysses_attention)
 
-__all__ = ["attention", "attention_chunked", "attention_online", "chunk_bounds", "head2seq",
+__all__ = ["attention", "attention_chunked", "attention_online", "attention_ring", "chunk_bounds",
+           "head2seq",
            "lse_merge", "seq2head", "softmax_weights", "to_f64", "ulysses_attention"]

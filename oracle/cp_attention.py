@@ -231,3 +231,35 @@ def ulysses_attention(q, k, v, P: int, scale: float | None = None):
     o, lse = attention(qh.reshape(Pg * B, Hl, S, D), kh.reshape(Pg * B, Hl, S, D),
                        vh.reshape(Pg * B, Hl, S, D), scale)
     return head2seq(o.reshape(Pg, B, Hl, S, D), P), lse.reshape(Pg, B, Hl, S)
+
+
+def attention_ring(q, k, v, P: int, scale: float | None = None):
+    """Ring Attention as the page's "Ring Attention" section (Figure 3) runs it: P ranks, rank r
+    holds query rows [floor(r*Sq/P), floor((r+1)*Sq/P)) and KV block r (``chunk_bounds``); at
+    ring step i = 0 .. P-1 it attends over the block it holds then, (r - i) mod P, and folds
+    the partial output into its running output with the log-sum-exp merge.
+
+    q [..., Sq, D], k/v [..., Skv, D] -> O [..., Sq, D], LSE [..., Sq] (float64).
+    """
+    q, k, v = to_f64(q), to_f64(k), to_f64(v)
+    Sq, Skv = q.shape[-2], k.shape[-2]
+    assert 1 <= P <= Skv
+    o = np.zeros(q.shape)
+    lse = np.full(q.shape[:-1], -np.inf)
+    for r in range(P):
+        q0, q1 = (r * Sq) // P, ((r + 1) * Sq) // P
+        if q1 == q0:
+            continue
+        qr = q[..., q0:q1, :]
+        o_run, lse_run = None, None
+        for i in range(P):
+            c = (r - i) % P
+            lo, hi = chunk_bounds(Skv, P, c)
+            o_c, lse_c = attention(qr, k[..., lo:hi, :], v[..., lo:hi, :], scale)
+            if o_run is None:
+                o_run, lse_run = o_c, lse_c
+            else:
+                o_run, lse_run = lse_merge(np.stack([o_run, o_c]), np.stack([lse_run, lse_c]))
+        o[..., q0:q1, :] = o_run
+        lse[..., q0:q1] = lse_run
+    return o, lse

@@ -172,3 +172,18 @@ def test_probe_argument_errors(L_):
     assert f(128, -1, 100, None) == E
     assert f(64, 2, 100, None) == E       # the step sequences need n = 128
     assert f(128, 0, 0, None) == E        # no iterations
+
+
+def ring(L_, P=4, q=A, k=B_, v=C, o=O, lse=L, B=1, H=2, Sq=256, Skv=256, D=64, dt=0):
+    return L_.attn_fwd_ring(q, k, v, P, o, lse, B, H, Sq, Skv, D, dt, 0.0, None)
+
+
+def test_ring_argument_errors(L_):
+    E, U, M = cpattn.ATTN_ERR_INVALID_ARG, cpattn.ATTN_ERR_UNSUPPORTED, cpattn.ATTN_ERR_MISALIGNED
+    assert ring(L_, P=0) == E
+    assert ring(L_, P=257) == E                     # more ranks than keys
+    assert ring(L_, D=96) == U
+    assert ring(L_, o=A + 16) == E                  # output inside q
+    assert ring(L_, lse=L + 4) == M
+    assert ring(L_, Sq=0) == cpattn.ATTN_OK         # nothing to compute
+    assert ring(L_, B=0, P=0) == E                  # P is still checked on an empty problem

@@ -333,6 +333,23 @@ def test_ulysses_equals_unsharded_attention():
     pin_ulysses(oracle.ulysses_attention)
 
 
+def pin_ring(ring):
+    """Ring Attention is exact: for any P (ragged ranks and chunks, fewer queries than ranks,
+    Sq != Skv) it gives the plain definition's O and LSE."""
+    for (Sq, Skv, P) in ((37, 53, 4), (8, 8, 8), (3, 29, 5), (64, 40, 1), (50, 50, 7)):
+        q = RNG.standard_normal((2, Sq, 8))
+        k = RNG.standard_normal((2, Skv, 8))
+        v = RNG.standard_normal((2, Skv, 8))
+        o_ref, lse_ref = oracle.attention(q, k, v)
+        o, lse = ring(q, k, v, P)
+        np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lse, lse_ref, rtol=1e-12, atol=1e-12)
+
+
+def test_ring_equals_plain_attention():
+    pin_ring(oracle.attention_ring)
+
+
 def test_raw_fp32_and_rounded_inputs_agree_to_bf16_precision():
     """tiny workload: the fp32 draw and its bf16 rounding give outputs within bf16 input error."""
     from context_math_non_b300.inputs import WORKLOADS, draw_qkv
@@ -424,6 +441,23 @@ def _mutants():
         y = x.reshape(P, B, Sl, H // P, P, D).transpose(4, 1, 3, 0, 2, 5)
         return np.ascontiguousarray(y.reshape(P, B, H // P, P * Sl, D))
 
+    def ring_missing_step(q, k, v, P):
+        # ring that stops one step early: the last block a rank would receive is never merged
+        q, k, v = (np.asarray(t, dtype=np.float64) for t in (q, k, v))
+        Sq, Skv = q.shape[-2], k.shape[-2]
+        o = np.zeros(q.shape)
+        lse = np.full(q.shape[:-1], -np.inf)
+        for r in range(P):
+            q0, q1 = (r * Sq) // P, ((r + 1) * Sq) // P
+            if q1 == q0:
+                continue
+            parts = [oracle.attention(q[..., q0:q1, :], k[..., lo:hi, :], v[..., lo:hi, :])
+                     for lo, hi in (oracle.chunk_bounds(Skv, P, (r - i) % P)
+                                    for i in range(max(1, P - 1)))]
+            om, lm = oracle.lse_merge(np.stack([a for a, _ in parts]), np.stack([b for _, b in parts]))
+            o[..., q0:q1, :], lse[..., q0:q1] = om, lm
+        return o, lse
+
     def ulysses_local_only(q, k, v, P):
         # no all-to-all: each rank attends over its own tokens only
         q, k, v = (np.asarray(t) for t in (q, k, v))
@@ -454,6 +488,7 @@ def _mutants():
         ("layout: swapped indices", lambda: pin_layout(s2h_swapped, oracle.head2seq)),
         ("layout: strided head split", lambda: pin_layout(s2h_head_order, oracle.head2seq)),
         ("ulysses: local attention only", lambda: pin_ulysses(ulysses_local_only)),
+        ("ring: one step short", lambda: pin_ring(ring_missing_step)),
         ("ulysses: batch-major LSE", lambda: pin_ulysses(ulysses_lse_batch_major)),
     ]
 
