@@ -252,6 +252,7 @@ def run_native(args, rank, world, local_rank):
     legs.update(_layout_leg(cpattn, dev, stream, peaks))
     legs.update(_ulysses_leg(cpattn, dev, stream))
     legs.update(_ring_leg(cpattn, qd, kd, vd, o, lse, dev, stream, flops, ms_per_step))
+    legs.update(_fp8_leg(cpattn, qd, kd, vd, o, lse, dev, stream, flops, peaks))
     clk = clocks.summary()
 
     e2e = None
@@ -462,6 +463,47 @@ def _ring_leg(cpattn, qd, kd, vd, o, lse, dev, stream, flops, step_ms, iters=5):
     return {"attn_fwd_ring_P8": {"median_ms": round(ms, 4),
                                  "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1),
                                  "vs_chunked_plus_merge_step_ms": round(step_ms, 4)}}
+
+
+def _fp8_leg(cpattn, qd, kd, vd, o, lse, dev, stream, flops, peaks, iters=5):
+    """The video problem in e4m3: per-tensor scales amax/448 (cp_absmax), quantisation
+    (cp_quantize_e4m3; V transposed), then attn_fwd_fp8 over P = 8 ring steps.  The attention
+    launch is timed alone; the quantisation of Q, K, V is reported beside it."""
+    scales = [cpattn.cp_absmax(t, stream=stream).item() / 448.0 for t in (qd, kd, vd)]
+    q8 = cpattn.cp_quantize_e4m3(qd, scales[0], stream=stream)
+    k8 = cpattn.cp_quantize_e4m3(kd, scales[1], stream=stream)
+    vt8 = cpattn.cp_quantize_e4m3(vd, scales[2], transpose=True, stream=stream)
+
+    def quant():
+        cpattn.cp_quantize_e4m3(qd, scales[0], out=q8, stream=stream)
+        cpattn.cp_quantize_e4m3(kd, scales[1], out=k8, stream=stream)
+        cpattn.cp_quantize_e4m3(vd, scales[2], transpose=True, out=vt8, stream=stream)
+
+    def attn():
+        cpattn.attn_fwd_fp8(q8, k8, vt8, P_CHUNKS, *scales, o=o, lse=lse, stream=stream)
+
+    out = {}
+    for name, fn in (("attention", attn), ("quantize_qkv", quant)):
+        fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(iters)]
+        for a, b in evs:
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        out[name] = statistics.median(a.elapsed_time(b) for a, b in evs)
+    st = cpattn.attn_device_status(stream)
+    if st != cpattn.ATTN_OK:
+        raise RuntimeError(f"device status after fp8 leg: {cpattn.attn_status_string(st)}")
+    tf = flops / (out["attention"] * 1e-3) / 1e12
+    fp8_peak = 2 * peaks["bf16"]   # dense e4m3 is twice the dense bf16 rate
+    del q8, k8, vt8
+    return {"attn_fwd_fp8_P8": {"median_ms": round(out["attention"], 4), "TFLOP/s": round(tf, 1),
+                                "frac_of_fp8_peak": round(tf / fp8_peak, 4),
+                                "fp8_peak_note": f"2 x {peaks['source']} burst dense bf16 "
+                                                 f"({peaks['bf16']}), the nominal e4m3/bf16 ratio",
+                                "quantize_qkv_ms": round(out["quantize_qkv"], 4)}}
 
 
 def _ulysses_leg(cpattn, dev, stream, iters=5):

@@ -14,7 +14,8 @@ from typing import Optional, Tuple
 import torch
 
 __all__ = ["CpAttnError", "CpAttnLibraryError", "lib", "attn_fwd", "attn_fwd_chunked",
-           "attn_lse_merge", "attn_fwd_ulysses", "attn_fwd_ring", "cp_layout_seq2head",
+           "attn_lse_merge", "attn_fwd_ulysses", "attn_fwd_ring", "attn_fwd_fp8", "cp_absmax",
+           "cp_quantize_e4m3", "cp_layout_seq2head",
            "cp_layout_head2seq", "attn_device_status",
            "attn_watchdog_selftest", "attn_set_max_ctas", "attn_probe_mma",
            "attn_set_kernel_variant", "attn_status_string", "attn_version",
@@ -61,6 +62,9 @@ def lib() -> ctypes.CDLL:
     L.attn_lse_merge.argtypes = [vp, fp, i, i, i, i, i, i, vp, fp, vp]
     L.attn_fwd_ulysses.argtypes = [vp, vp, vp, vp, fp, i, i, i, i, i, i, f, vp]
     L.attn_fwd_ring.argtypes = [vp, vp, vp, i, vp, fp, i, i, i, i, i, i, f, vp]
+    L.attn_fwd_fp8.argtypes = [vp, vp, vp, i, f, f, f, vp, fp, i, i, i, i, i, f, vp]
+    L.cp_absmax.argtypes = [vp, ctypes.c_longlong, i, fp, vp]
+    L.cp_quantize_e4m3.argtypes = [vp, i, vp, i, i, i, f, i, vp]
     L.cp_layout_seq2head.argtypes = [vp, vp, i, i, i, i, i, i, vp]
     L.cp_layout_head2seq.argtypes = [vp, vp, i, i, i, i, i, i, vp]
     L.attn_status_string.argtypes = [i]
@@ -72,7 +76,8 @@ def lib() -> ctypes.CDLL:
     L.attn_probe_mma.argtypes = [i, i, i, vp]
     L.attn_version.argtypes = []
     for name in ("attn_fwd", "attn_fwd_chunked", "attn_lse_merge", "attn_fwd_ulysses",
-                 "attn_fwd_ring", "cp_layout_seq2head", "cp_layout_head2seq",
+                 "attn_fwd_ring", "attn_fwd_fp8", "cp_absmax", "cp_quantize_e4m3",
+                 "cp_layout_seq2head", "cp_layout_head2seq",
                  "attn_device_status", "attn_watchdog_selftest", "attn_set_max_ctas",
                  "attn_version", "attn_probe_mma", "attn_set_kernel_variant"):
         getattr(L, name).restype = ctypes.c_int
@@ -183,6 +188,50 @@ def attn_fwd_ring(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int,
         _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), P, _dev(o, "o"), _ptr_or_null(lse, "lse"),
         B, H, Sq, Skv, D, _DT[q.dtype], float(scale), _stream(stream)))
     return o, lse
+
+
+def attn_fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, vt8: torch.Tensor, P: int, q_scale: float,
+                 k_scale: float, v_scale: float, o: Optional[torch.Tensor] = None,
+                 lse: Optional[torch.Tensor] = None, scale: float = 0.0, want_lse: bool = True,
+                 stream=None):
+    """e4m3 attention: q8 [B,H,Sq,D], k8 [B,H,Skv,D], vt8 [B,H,D,Skv] (one byte per element);
+    O bf16 [B,H,Sq,D], LSE [B,H,Sq]."""
+    B, H, Sq, D = q8.shape
+    Skv = k8.shape[2]
+    if o is None:
+        o = torch.empty((B, H, Sq, D), dtype=torch.bfloat16, device=q8.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q8.device)
+    _check("attn_fwd_fp8", lib().attn_fwd_fp8(
+        _dev(q8, "q"), _dev(k8, "k"), _dev(vt8, "vt"), P, float(q_scale), float(k_scale),
+        float(v_scale), _dev(o, "o"), _ptr_or_null(lse, "lse"), B, H, Sq, Skv, D, float(scale),
+        _stream(stream)))
+    return o, lse
+
+
+def cp_absmax(x: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """max |x| of a bf16/fp16 tensor, as a one-element fp32 device tensor."""
+    if out is None:
+        out = torch.empty((1,), dtype=torch.float32, device=x.device)
+    _check("cp_absmax", lib().cp_absmax(_dev(x, "x"), x.numel(), _DT[x.dtype], _dev(out, "amax"),
+                                        _stream(stream)))
+    return out
+
+
+def cp_quantize_e4m3(x: torch.Tensor, scale: float, transpose: bool = False,
+                     out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """e4m3 bytes of x / scale: x [..., S, D] -> [..., S, D], or [..., D, S] when transpose."""
+    *lead, S, D = x.shape
+    BH = 1
+    for d in lead:
+        BH *= d
+    if out is None:
+        shape = (*lead, D, S) if transpose else (*lead, S, D)
+        out = torch.empty(shape, dtype=torch.uint8, device=x.device)
+    _check("cp_quantize_e4m3", lib().cp_quantize_e4m3(
+        _dev(x, "x"), _DT[x.dtype], _dev(out, "y"), BH, S, D, float(scale), int(transpose),
+        _stream(stream)))
+    return out
 
 
 def attn_fwd_ulysses(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,

@@ -68,18 +68,20 @@ constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-template <int D>
+// kF8: e4m3 operands (one byte per element), so a 128-row tile of D = 128 is one 128-byte-wide
+// swizzled box of 16 KB, like a 16-bit tile of D = 64.
+template <int D, bool kF8 = false>
 struct Cfg {
-  static constexpr int NH = D / 64;                       // 64-wide halves per row
+  static constexpr int NH = kF8 ? 1 : D / 64;             // 128-byte-wide boxes per row
   static constexpr int TILE = NH * kHalfBytes;            // bytes of one 128-row tile
-  static constexpr int STAGES = (D == 128) ? 5 : 8;       // K/V ring depth
+  static constexpr int STAGES = (TILE == kHalfBytes) ? 8 : 5;   // K/V ring depth
   static constexpr int NBARS = 2 * STAGES + 10 * kQT + 2;
   static constexpr int SMEM = 1024 /*alignment slack*/ + kQT * TILE + STAGES * TILE +
                               NBARS * 8 + 16;
   static constexpr uint32_t S_COL0 = 0, S_COL1 = 128, O_COL0 = 256, O_COL1 = 256 + D;
   // D = 64 leaves 128 columns free: P gets its own columns, so S(j+1) can be computed while the
   // softmax of S(j) runs (separate-P schedule).  D = 128 writes P over the first half of S.
-  static constexpr bool SEP_P = (D == 64);
+  static constexpr bool SEP_P = (D == 64 && !kF8);
   static constexpr uint32_t P_COL0 = SEP_P ? 384 : S_COL0, P_COL1 = SEP_P ? 448 : S_COL1;
 };
 
@@ -87,7 +89,8 @@ struct Params {
   int Sq, Skv, P, BH, n_qb;
   int num_units;     // BH * P * n_qb (< 2^31, checked on the host)
   int kv_q, kv_r;    // Skv = kv_q * P + kv_r
-  float scale_log2;
+  float scale_log2;  // softmax scale * log2(e) (times the Q and K scales for e4m3 inputs)
+  float o_scale;     // output multiplier: 1, or the V scale for e4m3 inputs
   void* o;           // [P][BH][Sq][D]  (sequence-sharded layout: see SeqLayout)
   float* lse;        // [P][BH][Sq] or null
   unsigned long long limit_ns;
@@ -242,7 +245,8 @@ struct NoHook {
 // m_new), or 1), write P = 2^(s*scale*log2(e) - m) as 16-bit pairs to the 64 TMEM columns at
 // p_addr, and return the row sum of P.  kMasked treats columns >= valid as -inf (last tile of a
 // KV chunk).
-template <bool BF16, bool kMasked, typename AfterLoad = NoHook, typename BeforeStore = NoHook>
+template <bool BF16, bool kMasked, typename AfterLoad = NoHook, typename BeforeStore = NoHook,
+          bool kP8 = false>
 __device__ __forceinline__ float softmax_tile(uint32_t s_addr, uint32_t p_addr, float sl2,
                                               int valid, float& m, bool& need, float& alpha,
                                               AfterLoad after_load = AfterLoad(),
@@ -276,6 +280,28 @@ __device__ __forceinline__ float softmax_tile(uint32_t s_addr, uint32_t p_addr, 
   uint64_t lacc[4];
 #pragma unroll
   for (int a = 0; a < 4; ++a) lacc[a] = ptx::f2_pack(0.f, 0.f);
+  if constexpr (kP8) {
+    // P as e4m3, four per tensor-memory column (32 columns for the 128 keys)
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      uint32_t pk[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int e = 32 * h + 4 * c;
+        const uint64_t xa = ptx::f2_fma(ptx::f2_pack(SV(e), SV(e + 1)), sl2x2, negm2);
+        const uint64_t xb = ptx::f2_fma(ptx::f2_pack(SV(e + 2), SV(e + 3)), sl2x2, negm2);
+        float x0, x1, x2, x3;
+        ptx::f2_unpack(xa, x0, x1);
+        ptx::f2_unpack(xb, x2, x3);
+        const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1), p2 = ptx::ex2(x2), p3 = ptx::ex2(x3);
+        lacc[(2 * c) & 3] = ptx::f2_add(lacc[(2 * c) & 3], ptx::f2_pack(p0, p1));
+        lacc[(2 * c + 1) & 3] = ptx::f2_add(lacc[(2 * c + 1) & 3], ptx::f2_pack(p2, p3));
+        pk[c] = ptx::pack4_e4m3(p0, p1, p2, p3);
+      }
+      if (h == 0) before_store();
+      ptx::tmem_st8(p_addr + 8 * h, pk);
+    }
+  } else {
 #pragma unroll
   for (int h = 0; h < 4; ++h) {
     uint32_t pk[16];
@@ -291,6 +317,7 @@ __device__ __forceinline__ float softmax_tile(uint32_t s_addr, uint32_t p_addr, 
     }
     if (h == 0) before_store();
     ptx::tmem_st16(p_addr + 16 * h, pk);
+  }
   }
 #undef SV
   float la, lb;
@@ -326,12 +353,12 @@ __device__ __forceinline__ void rescale_o(uint32_t o_addr, float alpha) {
   }
 }
 
-template <int D, bool BF16, bool kSeq, bool kRing>
+template <int D, bool BF16, bool kSeq, bool kRing, bool kF8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const Params p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, kF8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -423,9 +450,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             ptx::mbar_arrive_expect_tx(&kv_full[st], C::TILE);
             const CUtensorMap* map = which == 0 ? &tm_k : &tm_v;
-            for (int h = 0; h < C::NH; ++h)
-              load_rows<kSeq>(sKV + st * C::TILE + h * kHalfBytes, map, 64 * h, kv_row, w.bh,
-                              &kv_full[st], p);
+            if (kF8 && which == 1) {
+              // V^T [BH][D][Skv]: the box is 128 keys (x, a multiple of 16 bytes) x D rows
+              ptx::tma_load_3d(sKV + st * C::TILE, map, kv_row, 0, w.bh, &kv_full[st]);
+            } else {
+              for (int h = 0; h < C::NH; ++h)
+                load_rows<kSeq>(sKV + st * C::TILE + h * kHalfBytes, map, 64 * h, kv_row, w.bh,
+                                &kv_full[st], p);
+            }
             ++kv_pos;
           }
         }
@@ -448,8 +480,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // each issuing warp is a serial chain of waits and issues, and splitting it halves the
     // chain per KV step.
     {
-      constexpr uint32_t kIdescS = ptx::idesc_f16(BF16, false, kBM, kBN);
-      constexpr uint32_t kIdescPV = ptx::idesc_f16(BF16, true, kBM, D);
+      // e4m3 (kF8): format code 0 in both operand fields and a K-major B (V^T) for P*V
+      constexpr uint32_t kIdescS = ptx::idesc_f16(kF8 ? false : BF16, false, kBM, kBN);
+      constexpr uint32_t kIdescPV = ptx::idesc_f16(kF8 ? false : BF16, !kF8, kBM, D);
       const uint32_t sQ_addr = ptx::smem_u32(sQ);
       const uint32_t sKV_addr = ptx::smem_u32(sKV);
 
@@ -459,22 +492,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_s = tmem + (t == 0 ? C::S_COL0 : C::S_COL1);
         const uint64_t da = ptx::smem_desc_sw128(a0, 16, 1024);
         const uint64_t db = ptx::smem_desc_sw128(b0, 16, 1024);
+        if constexpr (kF8) {
+          // K = 32 one-byte elements per MMA: 32-byte steps inside the 128-byte rows
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          // descriptor start-address field counts 16-byte units; no carry can leave it
-          const uint64_t off = static_cast<uint64_t>(((ks >> 2) * kHalfBytes + (ks & 3) * 32) >> 4);
-          ptx::mma_ss_elect(d_s, da + off, db + off, kIdescS, ks > 0);
+          for (int ks = 0; ks < D / 32; ++ks)
+            ptx::mma_ss_f8_elect(d_s, da + 2 * ks, db + 2 * ks, kIdescS, ks > 0);
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            // descriptor start-address field counts 16-byte units; no carry can leave it
+            const uint64_t off =
+                static_cast<uint64_t>(((ks >> 2) * kHalfBytes + (ks & 3) * 32) >> 4);
+            ptx::mma_ss_elect(d_s, da + off, db + off, kIdescS, ks > 0);
+          }
         }
       };
       auto issue_pv = [&](int t, uint32_t st, bool acc) {
         const uint32_t b0 = sKV_addr + st * C::TILE;
         const uint32_t d_o = tmem + (t == 0 ? C::O_COL0 : C::O_COL1);
         const uint32_t a_p = tmem + (t == 0 ? C::P_COL0 : C::P_COL1);
-        const uint64_t dv = ptx::smem_desc_sw128(b0, kHalfBytes, 1024);
+        if constexpr (kF8) {
+          // A = P (e4m3, 8 columns per 32 keys), B = the V^T tile, K-major over the keys
+          const uint64_t dvt = ptx::smem_desc_sw128(b0, 16, 1024);
 #pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks) {
-          ptx::mma_ts_elect(d_o, a_p + ks * 8, dv + static_cast<uint64_t>(ks * 128), kIdescPV,
-                            (acc || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < kBN / 32; ++ks)
+            ptx::mma_ts_f8_elect(d_o, a_p + ks * 8, dvt + 2 * ks, kIdescPV,
+                                 (acc || ks > 0) ? 1u : 0u);
+        } else {
+          const uint64_t dv = ptx::smem_desc_sw128(b0, kHalfBytes, 1024);
+#pragma unroll
+          for (int ks = 0; ks < kBN / 16; ++ks) {
+            ptx::mma_ts_elect(d_o, a_p + ks * 8, dv + static_cast<uint64_t>(ks * 128), kIdescPV,
+                              (acc || ks > 0) ? 1u : 0u);
+          }
         }
       };
 
@@ -652,10 +702,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float l_tile =
             valid < kBN
-                ? softmax_tile<BF16, true>(s_addr, p_addr, sl2, valid, m, need, alpha,
-                                           after_load, before_store)
-                : softmax_tile<BF16, false>(s_addr, p_addr, sl2, kBN, m, need, alpha, after_load,
-                                            before_store);
+                ? softmax_tile<BF16, true, decltype(after_load), decltype(before_store), kF8>(
+                      s_addr, p_addr, sl2, valid, m, need, alpha, after_load, before_store)
+                : softmax_tile<BF16, false, decltype(after_load), decltype(before_store), kF8>(
+                      s_addr, p_addr, sl2, kBN, m, need, alpha, after_load, before_store);
         if (!ok) break;
         l = l * alpha + l_tile;
         // Rescale O when the max moved in any row of this warp.  O is not in use: the P*V of
@@ -677,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       const int q_row = w.qb * (kQT * kBM) + t * kBM + row;
       const bool valid = q_row < p.Sq;
-      const float inv_l = 1.f / l;
+      const float inv_l = p.o_scale / l;
       const long long prow = static_cast<long long>(kRing ? 0 : w.c) * p.BH + w.bh;
       uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
                        out_row_offset<kSeq, D>(prow, w.bh, valid ? q_row : 0, p);
@@ -1122,23 +1172,23 @@ cudaError_t launch_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
   return cudaGetLastError();
 }
 
-template <int D, bool BF16, bool kSeq = false, bool kRing = false>
+template <int D, bool BF16, bool kSeq = false, bool kRing = false, bool kF8 = false>
 cudaError_t launch_typed(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const Params& p, int grid, cudaStream_t stream) {
-  auto kern = attn_fwd_kernel<D, BF16, kSeq, kRing>;
+  auto kern = attn_fwd_kernel<D, BF16, kSeq, kRing, kF8>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int regs = -1;
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    Cfg<D>::SMEM);
+                                    Cfg<D, kF8>::SMEM);
     cudaFuncAttributes fa;
     if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, kern);
     if (attr_err == cudaSuccess) regs = fa.numRegs;
   });
   if (attr_err != cudaSuccess) return attr_err;
   if (regs != kLaunchRegs) return cudaErrorInvalidKernelImage;   // see the register split
-  kern<<<grid, kThreads, Cfg<D>::SMEM, stream>>>(mq, mk, mv, p);
+  kern<<<grid, kThreads, Cfg<D, kF8>::SMEM, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -1185,6 +1235,7 @@ attn_status launch_attention(const void* q, const void* k, const void* v, void* 
   p.kv_q = Skv / P;
   p.kv_r = Skv % P;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.o_scale = 1.f;
   p.o = o;
   p.lse = lse;
   p.limit_ns = limit_ns;
@@ -1262,6 +1313,7 @@ attn_status launch_attention_ulysses(const void* q, const void* k, const void* v
   p.kv_q = S;
   p.kv_r = 0;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.o_scale = 1.f;
   p.o = o;
   p.lse = lse;
   p.limit_ns = limit_ns;
@@ -1279,6 +1331,58 @@ attn_status launch_attention_ulysses(const void* q, const void* k, const void* v
   else
     e = bf16 ? launch_typed<64, true, true>(mq, mk, mv, p, grid, stream)
              : launch_typed<64, false, true>(mq, mk, mv, p, grid, stream);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+namespace {
+// 3-D map over a one-byte tensor [BH][rows][cols] (cols contiguous, a multiple of 16), box =
+// 128 columns x 128 rows x 1, 128-byte swizzle.
+bool make_map_u8(CUtensorMap* map, const void* base, int cols, int rows, int BH) {
+  auto enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols),
+                           static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(cols)};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
+attn_status launch_attention_fp8(const void* q, const void* k, const void* vt, void* o,
+                                 float* lse, int P, int B, int H, int Sq, int Skv, float scale,
+                                 float q_scale, float k_scale, float v_scale, cudaStream_t stream,
+                                 unsigned long long limit_ns, int max_ctas) {
+  constexpr int D = 128;
+  const int BH = B * H;
+  int sms = device_sm_count();
+  if (sms <= 0) return ATTN_ERR_CUDA;
+  if (max_ctas > 0 && max_ctas < sms) sms = max_ctas;
+  CUtensorMap mq, mk, mv;
+  if (!make_map_u8(&mq, q, D, Sq, BH) || !make_map_u8(&mk, k, D, Skv, BH) ||
+      !make_map_u8(&mv, vt, Skv, D, BH))
+    return ATTN_ERR_CUDA;
+  Params p;
+  p.Sq = Sq;
+  p.Skv = Skv;
+  p.P = P;
+  p.BH = BH;
+  p.n_qb = (Sq + kQT * kBM - 1) / (kQT * kBM);
+  const long long units = static_cast<long long>(BH) * p.n_qb;
+  if (units >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+  p.num_units = static_cast<int>(units);
+  p.kv_q = Skv / P;
+  p.kv_r = Skv % P;
+  p.scale_log2 = scale * q_scale * k_scale * 1.4426950408889634f;
+  p.o_scale = v_scale;
+  p.o = o;
+  p.lse = lse;
+  p.limit_ns = limit_ns;
+  const int grid = p.num_units < sms ? p.num_units : sms;
+  const cudaError_t e = launch_typed<D, true, false, true, true>(mq, mk, mv, p, grid, stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

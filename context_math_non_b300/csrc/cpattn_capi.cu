@@ -143,6 +143,63 @@ attn_status attn_fwd_ulysses(const void* q, const void* k, const void* v, void* 
                                           cpattn::kDefaultWaitLimitNs, g_max_ctas.load());
 }
 
+attn_status attn_fwd_fp8(const void* q, const void* k, const void* vt, int P, float q_scale,
+                         float k_scale, float v_scale, void* o, float* lse, int B, int H, int Sq,
+                         int Skv, int D, float scale, attn_stream_t stream) {
+  if (!q || !k || !vt || !o) return ATTN_ERR_INVALID_ARG;
+  if (B < 0 || H < 0 || Sq < 0 || Skv < 1 || D < 1) return ATTN_ERR_INVALID_ARG;
+  if (P < 1 || P > Skv) return ATTN_ERR_INVALID_ARG;
+  for (float sc : {q_scale, k_scale, v_scale})
+    if (!(sc > 0.f) || !std::isfinite(sc)) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H > INT_MAX) return ATTN_ERR_INVALID_ARG;
+  if (D != 128) return ATTN_ERR_UNSUPPORTED;
+  // V^T rows are Skv bytes long and every KV tile starts at a multiple of 16 keys (the TMA
+  // alignment of one-byte elements): chunks must be equal and a multiple of 16 keys.
+  if (Skv % 16 != 0) return ATTN_ERR_UNSUPPORTED;
+  if (P > 1 && (Skv % P != 0 || (Skv / P) % 16 != 0)) return ATTN_ERR_UNSUPPORTED;
+  if (misaligned(q) || misaligned(k) || misaligned(vt) || misaligned(o) || misaligned(lse))
+    return ATTN_ERR_MISALIGNED;
+  if (B == 0 || H == 0 || Sq == 0) return ATTN_OK;
+  const long long bh = static_cast<long long>(B) * H;
+  const long long qbytes = bh * Sq * D, kvbytes = bh * Skv * D;
+  const long long obytes = qbytes * 2, lbytes = bh * Sq * 4;
+  for (const void* in : {q, k, vt}) {
+    const long long n = in == q ? qbytes : kvbytes;
+    if (overlaps(o, obytes, in, n) || overlaps(lse, lbytes, in, n)) return ATTN_ERR_INVALID_ARG;
+  }
+  if (overlaps(o, obytes, lse, lbytes)) return ATTN_ERR_INVALID_ARG;
+  return cpattn::launch_attention_fp8(q, k, vt, o, lse, P, B, H, Sq, Skv,
+                                      resolve_scale(scale, D), q_scale, k_scale, v_scale,
+                                      reinterpret_cast<cudaStream_t>(stream),
+                                      cpattn::kDefaultWaitLimitNs, g_max_ctas.load());
+}
+
+attn_status cp_absmax(const void* x, long long n, attn_dtype dt, float* amax,
+                      attn_stream_t stream) {
+  if (!x || !amax || n < 0 || !valid_dtype(dt)) return ATTN_ERR_INVALID_ARG;
+  if (n % 8 != 0) return ATTN_ERR_INVALID_ARG;
+  if (misaligned(x) || (reinterpret_cast<uintptr_t>(amax) & 3u) != 0) return ATTN_ERR_MISALIGNED;
+  if (overlaps(amax, 4, x, n * 2)) return ATTN_ERR_INVALID_ARG;
+  return cpattn::launch_absmax(x, n, dt == ATTN_BF16, amax,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status cp_quantize_e4m3(const void* x, attn_dtype dt, void* y, int BH, int S, int D,
+                             float scale, int transpose, attn_stream_t stream) {
+  if (!x || !y || BH < 0 || S < 0 || D < 1 || !valid_dtype(dt)) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (D % 16 != 0) return ATTN_ERR_INVALID_ARG;
+  if (transpose && (D % 64 != 0 || S % 16 != 0)) return ATTN_ERR_INVALID_ARG;
+  if (misaligned(x) || misaligned(y)) return ATTN_ERR_MISALIGNED;
+  const long long n = static_cast<long long>(BH) * S * D;
+  if (n == 0) return ATTN_OK;
+  if (overlaps(x, n * 2, y, n)) return ATTN_ERR_INVALID_ARG;
+  const float inv = 1.0f / scale;
+  if (!std::isfinite(inv)) return ATTN_ERR_INVALID_ARG;
+  return cpattn::launch_quantize_e4m3(x, dt == ATTN_BF16, y, BH, S, D, inv, transpose != 0,
+                                      reinterpret_cast<cudaStream_t>(stream));
+}
+
 attn_status attn_lse_merge(const void* o_parts, const float* lse_parts, int P, int B, int H,
                            int Sq, int D, attn_dtype dt, void* o, float* lse,
                            attn_stream_t stream) {

@@ -32,6 +32,20 @@ attn_status launch_attention_ulysses(const void* q, const void* k, const void* v
                                      float scale, cudaStream_t stream,
                                      unsigned long long limit_ns, int max_ctas);
 
+// e4m3 attention (D = 128) in ring mode over P chunks: q, k [B*H][S][128] e4m3, vt [B*H][128][Skv]
+// e4m3 (V transposed), real value = byte value * the tensor's scale; O bf16 [B*H][Sq][128].
+attn_status launch_attention_fp8(const void* q, const void* k, const void* vt, void* o,
+                                 float* lse, int P, int B, int H, int Sq, int Skv, float scale,
+                                 float q_scale, float k_scale, float v_scale, cudaStream_t stream,
+                                 unsigned long long limit_ns, int max_ctas);
+
+// max |x| of n 16-bit elements (n % 8 == 0) into *out (device fp32; zeroed first on `stream`).
+attn_status launch_absmax(const void* in, long long n, bool bf16, float* out, cudaStream_t stream);
+
+// y = e4m3(x * inv_scale): [BH][S][D] -> [BH][S][D], or -> [BH][D][S] when transpose.
+attn_status launch_quantize_e4m3(const void* in, bool bf16, void* out, int BH, int S, int D,
+                                 float inv_scale, bool transpose, cudaStream_t stream);
+
 attn_status launch_lse_merge(const void* o_parts, const float* lse_parts, int P, long long rows,
                              int D, bool bf16, void* o, float* lse, cudaStream_t stream);
 

@@ -1,0 +1,175 @@
+// Per-tensor e4m3 quantization for the FP8 attention path: the absolute maximum of a 16-bit
+// tensor (from which the caller picks the scale, e.g. amax / 448), and the conversion
+// y = e4m3(x * inv_scale) -- fp32 multiply, round to nearest even, saturate to +-448 -- either in
+// place order ([BH][S][D] -> [BH][S][D], for Q and K) or transposed per head ([BH][S][D] ->
+// [BH][D][S], for V: the P*V GEMM takes V as a K-major operand over the keys).
+// All three are HBM-bound streaming kernels.
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "cpattn_internal.h"
+#include "ptx_sm103.cuh"
+
+namespace cpattn {
+namespace {
+
+template <bool BF16>
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (BF16) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    } else {
+      const __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+      const float2 t = __half22float2(h);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+}
+
+// Grid-stride max of |x| over n16 16-byte vectors; one atomic per block on the bit pattern of
+// a non-negative float (ordered like the value).
+template <bool BF16>
+__global__ void __launch_bounds__(256) absmax_kernel(const uint4* __restrict__ in, long long n16,
+                                                     unsigned int* out) {
+  float m = 0.f;
+  for (long long i = blockIdx.x * 256ll + threadIdx.x; i < n16; i += gridDim.x * 256ll) {
+    float f[8];
+    unpack8<BF16>(__ldg(in + i), f);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(f[k]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ float wm[8];
+  if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float b = wm[0];
+    for (int w = 1; w < 8; ++w) b = fmaxf(b, wm[w]);
+    atomicMax(out, __float_as_uint(b));
+  }
+}
+
+// Same order: each thread converts 16 elements (two 16-byte loads, one 16-byte store).
+template <bool BF16>
+__global__ void __launch_bounds__(256) quantize_kernel(const uint4* __restrict__ in,
+                                                       uint4* __restrict__ out, long long n16x2,
+                                                       float inv_scale) {
+  for (long long i = blockIdx.x * 256ll + threadIdx.x; i < n16x2; i += gridDim.x * 256ll) {
+    float a[8], b[8];
+    unpack8<BF16>(__ldg(in + 2 * i), a);
+    unpack8<BF16>(__ldg(in + 2 * i + 1), b);
+    uint4 r;
+    r.x = ptx::pack4_e4m3(a[0] * inv_scale, a[1] * inv_scale, a[2] * inv_scale, a[3] * inv_scale);
+    r.y = ptx::pack4_e4m3(a[4] * inv_scale, a[5] * inv_scale, a[6] * inv_scale, a[7] * inv_scale);
+    r.z = ptx::pack4_e4m3(b[0] * inv_scale, b[1] * inv_scale, b[2] * inv_scale, b[3] * inv_scale);
+    r.w = ptx::pack4_e4m3(b[4] * inv_scale, b[5] * inv_scale, b[6] * inv_scale, b[7] * inv_scale);
+    out[i] = r;
+  }
+}
+
+// Transposed per head: block = one 64 (tokens) x 64 (features) tile of one head.  Loads are
+// 16-byte vectors along the features, stores 16-byte vectors of e4m3 along the tokens.
+constexpr int kT = 64;
+template <bool BF16>
+__global__ void __launch_bounds__(256) quantize_t_kernel(const uint16_t* __restrict__ in,
+                                                         uint8_t* __restrict__ out, int BH, int S,
+                                                         int D, float inv_scale) {
+  __shared__ __align__(16) uint8_t tile[kT][kT + 16];   // [feature][token], padded rows
+  const int s0 = blockIdx.x * kT, d0 = blockIdx.y * kT;
+  for (long long head = blockIdx.z; head < BH; head += gridDim.z) {
+  const uint16_t* src = in + head * S * static_cast<long long>(D);
+  uint8_t* dst = out + head * D * static_cast<long long>(S);
+  __syncthreads();   // the previous head's tile has been read out
+  // 64 tokens x 8 vectors of 8 features: 512 vectors, two per thread
+  for (int v = threadIdx.x; v < kT * (kT / 8); v += 256) {
+    const int sl = v >> 3, dv = (v & 7) * 8;
+    const int s = s0 + sl;
+    float f[8];
+    if (s < S) {
+      unpack8<BF16>(__ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(s) * D +
+                                                        d0 + dv)),
+                    f);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) f[k] = 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; k += 4) {
+      const uint32_t q = ptx::pack4_e4m3(f[k] * inv_scale, f[k + 1] * inv_scale,
+                                         f[k + 2] * inv_scale, f[k + 3] * inv_scale);
+#pragma unroll
+      for (int b = 0; b < 4; ++b) tile[dv + k + b][sl] = static_cast<uint8_t>(q >> (8 * b));
+    }
+  }
+  __syncthreads();
+  // 64 features x 4 vectors of 16 tokens: 256 vectors, one per thread
+  {
+    const int dl = threadIdx.x >> 2, sv = (threadIdx.x & 3) * 16;
+    const int s = s0 + sv;
+    if (s < S) {   // S is a multiple of 16, so a vector is either fully inside or outside
+      const uint4 r = *reinterpret_cast<const uint4*>(&tile[dl][sv]);
+      *reinterpret_cast<uint4*>(dst + static_cast<long long>(d0 + dl) * S + s) = r;
+    }
+  }
+  }
+}
+
+int grid_for(long long n, int sms) {
+  const long long blocks = (n + 255) / 256;
+  const long long cap = static_cast<long long>(sms) * 8;
+  return static_cast<int>(blocks < cap ? blocks : cap);
+}
+
+}  // namespace
+
+attn_status launch_absmax(const void* in, long long n, bool bf16, float* out,
+                          cudaStream_t stream) {
+  const int sms = device_sm_count();
+  if (sms <= 0) return ATTN_ERR_CUDA;
+  if (cudaMemsetAsync(out, 0, sizeof(float), stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  const long long n16 = n / 8;
+  const int grid = grid_for(n16, sms);
+  auto* o = reinterpret_cast<unsigned int*>(out);
+  if (bf16)
+    absmax_kernel<true><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(in), n16, o);
+  else
+    absmax_kernel<false><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(in), n16, o);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status launch_quantize_e4m3(const void* in, bool bf16, void* out, int BH, int S, int D,
+                                 float inv_scale, bool transpose, cudaStream_t stream) {
+  const int sms = device_sm_count();
+  if (sms <= 0) return ATTN_ERR_CUDA;
+  if (!transpose) {
+    const long long n16x2 = static_cast<long long>(BH) * S * D / 16;
+    const int grid = grid_for(n16x2, sms);
+    if (bf16)
+      quantize_kernel<true><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(in),
+                                                      static_cast<uint4*>(out), n16x2, inv_scale);
+    else
+      quantize_kernel<false><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(in),
+                                                       static_cast<uint4*>(out), n16x2, inv_scale);
+  } else {
+    const dim3 grid((S + kT - 1) / kT, D / kT, BH < 65535 ? BH : 65535);
+    if (bf16)
+      quantize_t_kernel<true><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(in),
+                                                        static_cast<uint8_t*>(out), BH, S, D,
+                                                        inv_scale);
+    else
+      quantize_t_kernel<false><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(in),
+                                                         static_cast<uint8_t*>(out), BH, S, D,
+                                                         inv_scale);
+  }
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace cpattn

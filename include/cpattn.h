@@ -139,6 +139,45 @@ CPATTN_API attn_status attn_fwd_ring(const void* q, const void* k, const void* v
                                      attn_dtype dt, float scale, attn_stream_t stream);
 
 /*
+ * attn_fwd_fp8 -- attention on e4m3 inputs with per-tensor scales (the 8-bit variant the pages
+ *   recommend for attention layers: page section on quantisation, "FP8 for attention").
+ *   Real inputs are q_scale*Q8, k_scale*K8, v_scale*V8.  S = Q8 K8^T and O = P8 V8 run on the
+ *   tensor cores in e4m3 with fp32 accumulation; the softmax is fp32 (logits times
+ *   scale*q_scale*k_scale); the softmax weights P are rounded to e4m3 (values in [0, 256],
+ *   round to nearest even) for the P*V product, while the denominator sums the fp32 weights.
+ *   The KV sequence is walked in P chunks in ring order exactly as attn_fwd_ring (P = 1: plain
+ *   attention).  Output O in bf16, O = v_scale * (P8 V8) / l.
+ *   q [B][H][Sq][D], k [B][H][Skv][D] e4m3 bytes; vt [B][H][D][Skv] e4m3 bytes (V transposed,
+ *   as cp_quantize_e4m3 with transpose = 1 writes it); o [B][H][Sq][D] bf16; lse [B][H][Sq]
+ *   fp32 or NULL (natural log of the sum of exp of the real scaled logits).
+ *   D = 128 and Skv % 16 == 0, and for P > 1 equal chunks of a multiple of 16 keys (Skv % P == 0,
+ *   (Skv/P) % 16 == 0): ATTN_ERR_UNSUPPORTED otherwise.  Scales must be positive and finite.
+ */
+CPATTN_API attn_status attn_fwd_fp8(const void* q, const void* k, const void* vt, int P,
+                                    float q_scale, float k_scale, float v_scale, void* o,
+                                    float* lse, int B, int H, int Sq, int Skv, int D, float scale,
+                                    attn_stream_t stream);
+
+/*
+ * cp_absmax -- *amax = max |x| over n bf16/fp16 elements (n % 8 == 0; x 16-byte aligned;
+ *   amax a device fp32, 4-byte aligned, zeroed by this call before the reduction).  For picking
+ *   an e4m3 scale (e.g. amax / 448).  Not part of the paper's method: input preparation for
+ *   attn_fwd_fp8.
+ */
+CPATTN_API attn_status cp_absmax(const void* x, long long n, attn_dtype dt, float* amax,
+                                 attn_stream_t stream);
+
+/*
+ * cp_quantize_e4m3 -- y = e4m3(x * (1/scale)), fp32 multiply, round to nearest even, saturating
+ *   to +-448 (NaN stays NaN).  x [BH][S][D] bf16/fp16; y [BH][S][D] bytes (transpose = 0) or
+ *   [BH][D][S] (transpose = 1, the V layout attn_fwd_fp8 takes).  D % 16 == 0; transposed:
+ *   D % 64 == 0 and S % 16 == 0 (ATTN_ERR_INVALID_ARG otherwise).  Input preparation for
+ *   attn_fwd_fp8.
+ */
+CPATTN_API attn_status cp_quantize_e4m3(const void* x, attn_dtype dt, void* y, int BH, int S,
+                                        int D, float scale, int transpose, attn_stream_t stream);
+
+/*
  * attn_fwd_ulysses -- DeepSpeed Ulysses attention without the two re-layout passes.
  *   Defines: page subsection "DeepSpeed Ulysses" and Figure 4 -- after the first all-to-all each
  *   rank attends over the full sequence for its subset of heads, and the second all-to-all

@@ -263,3 +263,91 @@ def attention_ring(q, k, v, P: int, scale: float | None = None):
         o[..., q0:q1, :] = o_run
         lse[..., q0:q1] = lse_run
     return o, lse
+
+
+# ------------------------------------------------------------------------------ e4m3 (FP8)
+# The 8-bit format the pages' quantisation section recommends for attention layers (FP8): e4m3
+# with 1 sign bit, 4 exponent bits (bias 7) and 3 mantissa bits, no infinities, the all-ones
+# pattern (S.1111.111) NaN, largest finite value 1.75 * 2^8 = 448, subnormals m/8 * 2^-6.
+
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(bits) -> np.ndarray:
+    """float64 value of e4m3 bytes (NaN for S.1111.111)."""
+    b = np.asarray(bits, dtype=np.uint8).astype(np.int64)
+    sign = np.where(b >> 7, -1.0, 1.0)
+    e = (b >> 3) & 15
+    m = (b & 7).astype(np.float64)
+    val = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7))
+    val = np.where((e == 15) & ((b & 7) == 7), np.nan, val)
+    return sign * val
+
+
+def e4m3_round(y) -> np.ndarray:
+    """Nearest e4m3 value to float64 y, ties to the even mantissa, finite overflow saturated to
+    +-448 (the saturating conversion); NaN stays NaN."""
+    y = np.asarray(y, dtype=np.float64)
+    a = np.abs(y)
+    # spacing of the e4m3 grid around a: 2^-9 below 2^-6 (subnormals), 2^(e-3) in binade e
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, -6.0)
+    step = np.exp2(e - 3)
+    q = np.round(a / step) * step          # numpy rounds halves to even
+    q = np.minimum(q, E4M3_MAX)
+    q = np.where(np.isnan(y), np.nan, q)
+    return np.copysign(q, y)
+
+
+def e4m3_encode(vals) -> np.ndarray:
+    """Bytes of values that are exactly representable in e4m3 (output of e4m3_round)."""
+    v = np.asarray(vals, dtype=np.float64)
+    sign = np.signbit(v).astype(np.int64) << 7
+    a = np.abs(v)
+    sub = a < 2.0 ** -6
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0))).astype(np.int64)
+    e = np.maximum(e, -6)
+    m_norm = np.round((a / np.exp2(e) - 1.0) * 8).astype(np.int64)
+    m_sub = np.round(a / 2.0 ** -9).astype(np.int64)
+    code = np.where(sub, m_sub, ((e + 7) << 3) | m_norm)
+    code = np.where(np.isnan(v), 0x7F, code)
+    return (sign | np.where(np.isnan(v), 0x7F, code)).astype(np.uint8)
+
+
+def e4m3_quantize(x, scale: float) -> np.ndarray:
+    """Bytes of e4m3(x * (1/scale)) as the quantisation step computes it: 1/scale rounded to
+    fp32, the product rounded to fp32, then rounded to e4m3."""
+    inv = np.float32(1.0) / np.float32(scale)
+    y = (to_f64(x).astype(np.float32) * inv).astype(np.float64)
+    return e4m3_encode(e4m3_round(y))
+
+
+def attention_fp8(q8, k8, v8, q_scale: float, k_scale: float, v_scale: float,
+                  scale: float | None = None):
+    """Exact attention on the real values the e4m3 inputs stand for (byte value times the
+    tensor's scale).  v8 in the natural [..., Skv, D] order.  Returns O, LSE (float64)."""
+    q = e4m3_decode(q8) * q_scale
+    k = e4m3_decode(k8) * k_scale
+    v = e4m3_decode(v8) * v_scale
+    return attention(q, k, v, scale)
+
+
+def fp8_p_rounding_bound(q8, k8, v8, q_scale: float, k_scale: float, v_scale: float,
+                         scale: float | None = None) -> np.ndarray:
+    """Worst-case |O error| per element from rounding the softmax weights to e4m3 before P*V.
+
+    With p_j = exp(s_j - m) for any running max m <= max_j s_j (so p_j <= 2^8 < 448: no
+    saturation), rounding to nearest e4m3 moves p_j by at most max(2^-4 p_j, 2^-10) (half a
+    step: relative 2^-4 for normal values, absolute 2^-10 among subnormals).  With l = sum p_j
+    >= l_min = sum exp(s_j - max s) the output O = sum p_j v_j / l moves by at most
+    sum_j (2^-4 w_j + 2^-10 / l_min) |v_j| (w = softmax weights).  Shape [..., Sq, D].
+    """
+    q = e4m3_decode(q8) * q_scale
+    k = e4m3_decode(k8) * k_scale
+    v = np.abs(e4m3_decode(v8) * v_scale)
+    sc = _default_scale(q.shape[-1]) if scale is None else scale
+    s = np.einsum("...qd,...kd->...qk", q, k) * sc         # [..., Sq, Skv]
+    e = np.exp(s - s.max(axis=-1, keepdims=True))
+    l_min = e.sum(axis=-1)
+    w = e / l_min[..., None]
+    return 2.0 ** -4 * (w @ v) + (2.0 ** -10 / l_min)[..., None] * v.sum(axis=-2)[..., None, :]

@@ -56,7 +56,7 @@ def test_library_exports_nothing_undeclared(L_):
     out = subprocess.run(["nm", "-D", "--defined-only", cpattn.LIB_PATH], capture_output=True,
                          text=True).stdout
     exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
-    ours = {s for s in exported if s.startswith(("attn_", "cp_layout_"))}
+    ours = {s for s in exported if s.startswith(("attn_", "cp_"))}
     assert ours == set(declared_functions())
 
 
@@ -187,3 +187,37 @@ def test_ring_argument_errors(L_):
     assert ring(L_, lse=L + 4) == M
     assert ring(L_, Sq=0) == cpattn.ATTN_OK         # nothing to compute
     assert ring(L_, B=0, P=0) == E                  # P is still checked on an empty problem
+
+
+def fp8(L_, q=A, k=B_, vt=C, P=1, qs=0.01, ks=0.01, vs=0.01, o=O, lse=L, B=1, H=2, Sq=256,
+        Skv=256, D=128):
+    return L_.attn_fwd_fp8(q, k, vt, P, qs, ks, vs, o, lse, B, H, Sq, Skv, D, 0.0, None)
+
+
+def test_fp8_argument_errors(L_):
+    E, U, M = cpattn.ATTN_ERR_INVALID_ARG, cpattn.ATTN_ERR_UNSUPPORTED, cpattn.ATTN_ERR_MISALIGNED
+    assert fp8(L_, D=64) == U                      # e4m3 path is D = 128
+    assert fp8(L_, Skv=250) == U                   # V^T rows must be a multiple of 16 bytes
+    assert fp8(L_, P=7, Skv=256) == U              # unequal chunks
+    assert fp8(L_, P=2, Skv=48) == U               # 24-key chunks: not a multiple of 16
+    assert fp8(L_, qs=0.0) == E
+    assert fp8(L_, vs=float("inf")) == E
+    assert fp8(L_, P=0) == E
+    assert fp8(L_, o=A + 1024) == E                # output inside q
+    assert fp8(L_, k=B_ + 8) == M
+    assert fp8(L_, Sq=0) == cpattn.ATTN_OK
+
+
+def test_quantize_argument_errors(L_):
+    E, M = cpattn.ATTN_ERR_INVALID_ARG, cpattn.ATTN_ERR_MISALIGNED
+    f = L_.cp_quantize_e4m3
+    assert f(A, 0, O, 2, 64, 100, 0.5, 0, None) == E        # D not a multiple of 16
+    assert f(A, 0, O, 2, 40, 128, 0.5, 1, None) == E        # transposed: S multiple of 16
+    assert f(A, 0, O, 2, 64, 96, 0.5, 1, None) == E         # transposed: D multiple of 64
+    assert f(A, 0, O, 2, 64, 128, 0.0, 0, None) == E        # scale must be positive
+    assert f(A, 0, A + 64, 2, 64, 128, 0.5, 0, None) == E   # output overlaps input
+    assert f(A + 4, 0, O, 2, 64, 128, 0.5, 0, None) == M
+    assert f(A, 0, O, 0, 64, 128, 0.5, 0, None) == cpattn.ATTN_OK
+    g = L_.cp_absmax
+    assert g(A, 12, 0, L, None) == E                        # n must be a multiple of 8
+    assert g(A, 16, 0, L + 2, None) == M

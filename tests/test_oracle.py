@@ -350,6 +350,84 @@ def test_ring_equals_plain_attention():
     pin_ring(oracle.attention_ring)
 
 
+def test_e4m3_decode_all_codes():
+    """Every e4m3 byte against torch's float8_e4m3fn decoding (a library routine), and the
+    format's landmarks by hand."""
+    codes = np.arange(256, dtype=np.uint8)
+    d = oracle.e4m3_decode(codes)
+    t = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert (np.isnan(d) == np.isnan(t)).all()
+    np.testing.assert_array_equal(np.nan_to_num(d), np.nan_to_num(t))
+    assert oracle.e4m3_decode(0x7E) == 448.0 and oracle.e4m3_decode(0xFE) == -448.0
+    assert oracle.e4m3_decode(0x38) == 1.0 and oracle.e4m3_decode(0x08) == 2.0 ** -6
+    assert oracle.e4m3_decode(0x01) == 2.0 ** -9 and np.isnan(oracle.e4m3_decode(0x7F))
+
+
+def pin_e4m3_round(rnd):
+    """Round-to-nearest-even onto the e4m3 grid with saturation: torch's conversion for values
+    inside the range, hand-made ties, subnormals and overflow."""
+    x = np.concatenate([RNG.standard_normal(20000) * 60, RNG.standard_normal(5000) * 0.01,
+                        RNG.uniform(-448, 448, 5000)])
+    got = oracle.e4m3_encode(rnd(x))
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(got, ref)
+    cases = {1.0625: 1.0, 1.1875: 1.25, 2.0 ** -10: 0.0, 3 * 2.0 ** -10: 2.0 ** -8,
+             -1.0625: -1.0, 464.0: 448.0, 500.0: 448.0, -1e6: -448.0, 0.0: 0.0, 2.0 ** -20: 0.0,
+             1.96875: 2.0, 240.0: 240.0, 248.0: 256.0}
+    for v, want in cases.items():
+        assert rnd(np.array([v]))[0] == want, (v, rnd(np.array([v]))[0], want)
+
+
+def test_e4m3_round_and_encode():
+    pin_e4m3_round(oracle.e4m3_round)
+
+
+def test_e4m3_quantize_is_fp32_scale_then_round():
+    g = torch.Generator().manual_seed(5)
+    x = (torch.randn(4096, generator=g) * 3).to(torch.bfloat16)
+    scale = 0.0123
+    got = oracle.e4m3_quantize(x, scale)
+    inv = torch.tensor(1.0, dtype=torch.float32) / torch.tensor(scale, dtype=torch.float32)
+    y = x.float() * inv
+    ref = y.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    inside = (y.abs() <= 448).numpy()   # torch turns overflow into NaN; the quantiser saturates
+    assert inside.sum() > 3000 and (~inside).sum() > 50
+    np.testing.assert_array_equal(got[inside], ref[inside])
+    np.testing.assert_array_equal(got[~inside], np.where(y.numpy()[~inside] > 0, 0x7E, 0xFE))
+
+
+def simulate_p8_error(q, k, v, lag):
+    """Attention with the softmax weights rounded to e4m3 relative to a running max `lag` below
+    the true max (as the kernel's lazy rescale allows), against exact attention."""
+    s = q @ k.T / math.sqrt(q.shape[-1])
+    m = s.max(axis=-1, keepdims=True) - lag
+    p = np.exp(s - m)
+    pq = oracle.e4m3_round(p)
+    o_q = (pq @ v) / p.sum(axis=-1, keepdims=True)
+    o = (p @ v) / p.sum(axis=-1, keepdims=True)
+    return np.abs(o_q - o)
+
+
+def pin_p8_bound(bound_fn):
+    """The e4m3 P-rounding bound holds in direct simulation, including rows dominated by
+    subnormal weights and a running max up to 8 (log2) below the true max."""
+    for trial, (Sq, Skv, spread) in enumerate(((16, 64, 1.0), (16, 300, 6.0), (8, 1000, 0.3))):
+        D = 16
+        q = RNG.standard_normal((Sq, D)) * spread
+        k = RNG.standard_normal((Skv, D))
+        v = RNG.standard_normal((Skv, D))
+        q8, k8, v8 = (oracle.e4m3_encode(oracle.e4m3_round(t)) for t in (q, k, v))
+        qd, kd, vd = (oracle.e4m3_decode(t) for t in (q8, k8, v8))
+        bound = bound_fn(q8, k8, v8, 1.0, 1.0, 1.0)
+        for lag in (0.0, 3.3, 8.0 * math.log(2.0)):
+            err = simulate_p8_error(qd, kd, vd, lag)
+            assert (err <= bound * (1 + 1e-9) + 1e-12).all(), (trial, lag, (err - bound).max())
+
+
+def test_fp8_p_rounding_bound():
+    pin_p8_bound(oracle.fp8_p_rounding_bound)
+
+
 def test_raw_fp32_and_rounded_inputs_agree_to_bf16_precision():
     """tiny workload: the fp32 draw and its bf16 rounding give outputs within bf16 input error."""
     from context_math_non_b300.inputs import WORKLOADS, draw_qkv
@@ -458,6 +536,21 @@ def _mutants():
             o[..., q0:q1, :], lse[..., q0:q1] = om, lm
         return o, lse
 
+    def round_toward_zero(y):
+        y = np.asarray(y, dtype=np.float64)
+        a = np.abs(y)
+        e = np.maximum(np.floor(np.log2(np.where(a > 0, a, 1.0))), -6.0)
+        step = np.exp2(e - 3)
+        return np.copysign(np.minimum(np.floor(a / step) * step, 448.0), y)
+
+    def p8_bound_too_tight(q8, k8, v8, qs, ks, vs):
+        # relative half-step of 2^-6 instead of 2^-4 and no subnormal term
+        b = oracle.fp8_p_rounding_bound(q8, k8, v8, qs, ks, vs)
+        q = oracle.e4m3_decode(q8)
+        k = oracle.e4m3_decode(k8)
+        w = oracle.softmax_weights(q, k)
+        return 2.0 ** -6 * (w @ np.abs(oracle.e4m3_decode(v8))) + 0 * b
+
     def ulysses_local_only(q, k, v, P):
         # no all-to-all: each rank attends over its own tokens only
         q, k, v = (np.asarray(t) for t in (q, k, v))
@@ -489,6 +582,8 @@ def _mutants():
         ("layout: strided head split", lambda: pin_layout(s2h_head_order, oracle.head2seq)),
         ("ulysses: local attention only", lambda: pin_ulysses(ulysses_local_only)),
         ("ring: one step short", lambda: pin_ring(ring_missing_step)),
+        ("e4m3: rounds toward zero", lambda: pin_e4m3_round(round_toward_zero)),
+        ("e4m3: P bound too tight", lambda: pin_p8_bound(p8_bound_too_tight)),
         ("ulysses: batch-major LSE", lambda: pin_ulysses(ulysses_lse_batch_major)),
     ]
 
