@@ -144,3 +144,18 @@ def test_fp8_gpu_quantizer_feeds_the_same_attention():
     o1, l1 = cpattn.attn_fwd_fp8(gq, gk, gvt, 2, *scales)
     o2, l2 = cpattn.attn_fwd_fp8(*(torch.from_numpy(t).cuda() for t in (q8, k8, vt8)), 2, *scales)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_fp8_attention_large_logits():
+    """Q x4 and a few K rows x8 (the stress recipe): logits far above 1, the running max jumps
+    between tiles; the P-rounding bound still applies (P <= 2^8 after the lazy rescale)."""
+    g = torch.Generator().manual_seed(123)
+    q = (torch.randn(1, 2, 256, 128, generator=g) * 4).to(torch.bfloat16)
+    k = torch.randn(1, 2, 2048, 128, generator=g)
+    k[:, :, torch.randperm(2048, generator=g)[:20]] *= 8
+    k = k.to(torch.bfloat16)
+    v = torch.randn(1, 2, 2048, 128, generator=g).to(torch.bfloat16)
+    (q8, k8, v8, vt8), scales = quantized_inputs(q, k, v)
+    o, lse = cpattn.attn_fwd_fp8(*(torch.from_numpy(t).cuda() for t in (q8, k8, vt8)), 4, *scales)
+    assert cpattn.attn_device_status() == cpattn.ATTN_OK
+    check_fp8(o.cpu(), lse.cpu(), q8, k8, v8, scales, what="fp8 large logits")

@@ -83,3 +83,26 @@ def test_ring_video_sampled():
     o_ref, lse_ref = oracle_rows(q, k, v, rows)
     assert_attention_close(o[:, :, rows].cpu(), lse[:, :, rows].cpu(), o_ref, lse_ref,
                            "video ring P=8")
+
+
+def test_ring_stress_sampled():
+    """stress: B=1 H=16 S=32768, Q x4 and 1 % of K rows x8 (logits up to ~150), P = 8 ring steps:
+    the running max jumps by far more than the lazy-rescale threshold between chunks."""
+    w = WORKLOADS["stress"]
+    q, k, v = draw_qkv(w)
+    o, lse = cpattn.attn_fwd_ring(q.cuda(), k.cuda(), v.cuda(), 8)
+    assert cpattn.attn_device_status() == cpattn.ATTN_OK
+    rows = sample_rows(w.S, 24, seed=w.seed + 3, extra=(4095, 4096, 4097))
+    o_ref, lse_ref = oracle_rows(q, k, v, rows)
+    assert_attention_close(o[:, :, rows].cpu(), lse[:, :, rows].cpu(), o_ref, lse_ref,
+                           "stress ring P=8")
+
+
+@pytest.mark.parametrize("P", [16, 64])
+def test_ring_many_ranks_fp16(P):
+    """Many short chunks (ragged: 2000 keys over 16 / 64 ranks), fp16, both D."""
+    for D in (64, 128):
+        q, k, v = rand_qkv(1, 2, 700, 2000, D, torch.float16, seed=P + D)
+        o, lse = cpattn.attn_fwd_ring(q.cuda(), k.cuda(), v.cuda(), P)
+        o_ref, lse_ref = oracle.attention_ring(q, k, v, P)
+        assert_attention_close(o, lse, o_ref, lse_ref, f"ring P={P} D={D} fp16")

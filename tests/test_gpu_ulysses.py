@@ -109,3 +109,16 @@ def test_ulysses_full_size_sampled():
                                                                              len(rows), D)
     lse_got = lse.view(Pg * B, Hl, S)[:, :, torch.as_tensor(rows)].cpu()
     assert_attention_close(got, lse_got, o_ref, lse_ref, "ulysses full size")
+
+
+def test_ulysses_bf16_d128_ragged():
+    """bf16, D = 128, S/P = 112 (16-token boxes), last tile ragged; bit-equal to the unfused
+    chain and within tolerance of the oracle."""
+    P, B, S, H, D = 4, 2, 448, 8, 128
+    q, k, v = draw(P, B, S, H, D, torch.bfloat16, seed=31)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o, lse = cpattn.attn_fwd_ulysses(qd, kd, vd)
+    o_ref, lse_ref = oracle.ulysses_attention(q, k, v, P)
+    assert_attention_close(o, lse, o_ref, lse_ref, "ulysses bf16 D128")
+    o_u, lse_u = unfused(qd, kd, vd)
+    assert torch.equal(o, o_u) and torch.equal(lse, lse_u)
