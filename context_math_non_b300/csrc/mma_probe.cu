@@ -4,7 +4,7 @@
 // thread issues `iters` kind::f16 MMAs (M = 128, N = n, K = 16, fp32 accumulation) -- operands
 // from shared memory (SS) or A from tensor memory (TS), the two forms the attention kernel uses
 // for S = Q K^T and O += P V.  Timing the launch gives the achievable MMA rate of each form,
-// the denominator against which the attention kernel's pipeline is judged.  Mode "step" issues
+// the denominator against which the attention kernel's pipeline is measured.  Mode "step" issues
 // the attention kernel's per-KV-step sequence instead (P0*V, Q0*K^T, P1*V, Q1*K^T with N = 128,
 // alternating accumulators, one commit after each GEMM), counting 4 GEMMs of 8 MMAs per step.
 
