@@ -731,28 +731,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long prow = static_cast<long long>(kRing ? 0 : w.c) * p.BH + w.bh;
       uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
                        out_row_offset<kSeq, D>(prow, w.bh, valid ? q_row : 0, p);
-#pragma unroll
-      for (int half = 0; half < D / 64; ++half) {
-        uint32_t orr[64];
-        ptx::tmem_ld64(o_addr + 64 * half, orr);
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 64 * half);
-#pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-              pk[c] = ptx::pack2<BF16>(__uint_as_float(orr[8 * v + 2 * c]) * inv_l,
-                                       __uint_as_float(orr[8 * v + 2 * c + 1]) * inv_l);
-            dst[v] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          }
-        }
-      }
-      if (valid && p.lse != nullptr)
-        p.lse[prow * p.Sq + q_row] = (m + __log2f(l)) * 0.69314718055994530942f;
+      // The whole O row goes to registers first, so the accumulator is released (o_empty)
+      // before the normalisation and the global stores: the next output's first P*V, which
+      // overwrites O, waits only for the tensor-memory reads.
+      uint32_t orr[D];
+      tmem_ld_cols<D>(o_addr, orr);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&o_empty[t]);
+      if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+        for (int v = 0; v < D / 8; ++v) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            pk[c] = ptx::pack2<BF16>(__uint_as_float(orr[8 * v + 2 * c]) * inv_l,
+                                     __uint_as_float(orr[8 * v + 2 * c + 1]) * inv_l);
+          dst[v] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+        if (p.lse != nullptr)
+          p.lse[prow * p.Sq + q_row] = (m + __log2f(l)) * 0.69314718055994530942f;
+      }
     }
   }
 
