@@ -189,3 +189,26 @@ def test_long_sequence_workloads_sampled(name):
     om_ref, lm_ref = oracle.lse_merge(to_np(op[:, :, :, rows]), to_np(lp[:, :, :, rows]))
     assert_attention_close(om[:, :, rows].cpu(), lm[:, :, rows].cpu(), om_ref, lm_ref,
                            f"{name} merge of GPU partials")
+
+
+def test_very_long_sequence_sampled():
+    """One head of 262144 tokens (D = 64, bf16), KV in P = 3 ragged chunks (87381 / 87381 /
+    87382 keys): long units, far offsets in O and LSE; sampled rows against the oracle, for the
+    partials, their merge, and the fused ring."""
+    S = 262144
+    g = torch.Generator().manual_seed(262144)
+    q, k, v = (torch.randn(1, 1, S, 64, generator=g).to(torch.bfloat16) for _ in range(3))
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    op, lp = cpattn.attn_fwd_chunked(qd, kd, vd, 3)
+    om, lm = cpattn.attn_lse_merge(op, lp)
+    orr, lrr = cpattn.attn_fwd_ring(qd, kd, vd, 3)
+    assert cpattn.attn_device_status() == cpattn.ATTN_OK
+    rows = sample_rows(S, 10, seed=9, extra=(87380, 87381, 174762, 174763))
+    op_ref, lp_ref = oracle_rows(q, k, v, rows, 3)
+    assert_attention_close(op[:, :, :, rows].cpu(), lp[:, :, :, rows].cpu(), op_ref, lp_ref,
+                           "262144 tokens, partials")
+    o_ref, lse_ref = oracle_rows(q, k, v, rows)
+    assert_attention_close(om[:, :, rows].cpu(), lm[:, :, rows].cpu(), o_ref, lse_ref,
+                           "262144 tokens, merged")
+    assert_attention_close(orr[:, :, rows].cpu(), lrr[:, :, rows].cpu(), o_ref, lse_ref,
+                           "262144 tokens, ring")
