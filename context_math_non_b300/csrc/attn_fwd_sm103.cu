@@ -5,25 +5,33 @@
 // ("Scaling AI Inference Across Multiple GPUs Using NVIDIA TensorRT with Multi-Device Inference
 // Support", subsection "Ring Attention", Figure 3) -- with an online softmax, so the full score
 // matrix never exists anywhere.  Outputs: O normalised over the range, and the range's
-// natural-log LSE.
+// natural-log LSE.  Variants of the same kernel (template parameters): the sequence-sharded
+// (Ulysses) addressing (kSeq), the ring walk over all P chunks with the merge on chip (kRing),
+// and e4m3 operands (kF8).
 //
-// Work unit: (chunk c, batch*head bh, 256-query block qb).  A persistent grid of one CTA per SM
-// walks the units in a static round-robin; consecutive units share (bh, c), so the CTAs resident
-// at one time read the same K/V chunk and L2 serves the re-reads.
+// Work unit: (chunk c, batch*head bh, 256-query block qb); in ring mode (bh, qb) over all chunks.
+// A persistent grid of one CTA per SM walks the units in a static round-robin; consecutive units
+// share (bh, c), so the CTAs resident at one time read the same K/V chunk and L2 serves the
+// re-reads.
 //
 // CTA roles (384 threads = 3 warpgroups):
 //   warps 0-3  softmax for query tile 0 (thread = row; TMEM lanes 0..127)
 //   warps 4-7  softmax for query tile 1
 //   warp  8    TMA producer: Q tiles once per unit, then K_j / V_j through a ring of stages
-//   warp  9    TMEM allocation and the single MMA-issuing thread
-//   warps 10-11 idle (they complete the third warpgroup, which releases registers to the
-//              softmax warpgroups with setmaxnreg)
-// Tensor memory (512 columns): S0 | S1 | O0 | O1.  P (16-bit) is written over the first half of
-// its S columns and read from TMEM by the P*V MMA.  The MMA order per KV step j
+//   warp  9    TMEM allocation and MMA issue: the whole warp runs the loop (waits voted across
+//              the warp) and one elected lane issues, so the operands stay warp-uniform
+//   warp  10   with separate P (D = 64): issues the O += P V GEMMs while warp 9 issues S
+//   warps 10-11 otherwise idle (they complete the third warpgroup, which releases registers to
+//              the softmax warpgroups with setmaxnreg)
+// Tensor memory (512 columns): S0 | S1 | O0 | O1.  For D = 128, P (16-bit, or e4m3) is written
+// over the first part of its S columns and read from TMEM by the P*V MMA.  The MMA order per KV
+// step j
 //   O0 += P0 V_{j-1};  S0 = Q0 K_j^T;  O1 += P1 V_{j-1};  S1 = Q1 K_j^T
 // lets each softmax warpgroup work on its tile while the tensor core runs the other tile's two
-// GEMMs.  The running max is only moved (and O rescaled) when it grows by more than 2^8, so most
-// steps skip the rescale; the final normalisation uses the same stale max, so results are exact.
+// GEMMs.  For D = 64 the O regions are half as wide and P gets its own columns, so S_t(j+1) is
+// computed while the softmax of S_t(j) runs (separate-P schedule).  The running max is only moved
+// (and O rescaled) when it grows by more than 2^8, so most steps skip the rescale; the final
+// normalisation uses the same stale max, so results are exact.
 //
 // Every wait is bounded (see mbar_wait): a lost signal ends the kernel with ATTN_ERR_TIMEOUT in
 // the status word instead of a hang.
@@ -772,7 +780,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // S = Q K^T, a V tile for O += P V) is split along N between the two CTAs.  So each CTA loads
 // only half of every K/V tile (K: 64 of the 128 KV rows; V: 64 of the 128 columns of D) and
 // reads only its half from shared memory for the MMA: shared-memory traffic for B operands and
-// TMA writes per SM are halved, which is what limits the single-CTA kernel.
+// TMA writes per SM are halved (TMA writes competing with the MMA operand reads cost the
+// single-CTA kernel 5-10 %).  The cross-SM hand-offs cost more than that saves, so this variant
+// is slower and not the default (attn_set_kernel_variant).
 //
 // Unit: (chunk, batch*head, 512-query block); CTA r of the pair owns query rows
 // [256 r, 256 r + 256) of the block as two 128-row tiles, exactly like the single-CTA kernel.
