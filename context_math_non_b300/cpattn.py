@@ -125,6 +125,23 @@ def _ptr_or_null(t: Optional[torch.Tensor], name: str):
     return None if t is None else _dev(t, name)
 
 
+def _dt(t: torch.Tensor, name: str) -> int:
+    """Library dtype code of a 16-bit float tensor."""
+    if t.dtype not in _DT:
+        raise ValueError(f"{name} must be bfloat16 or float16, not {t.dtype}")
+    return _DT[t.dtype]
+
+
+_BYTE_TYPES = (torch.uint8,) + ((torch.float8_e4m3fn,) if hasattr(torch, "float8_e4m3fn") else ())
+
+
+def _e4m3(t: torch.Tensor, name: str) -> int:
+    """Pointer of a tensor of e4m3 bytes (uint8 or float8_e4m3fn)."""
+    if t.dtype not in _BYTE_TYPES:
+        raise ValueError(f"{name} must hold e4m3 bytes (uint8 or float8_e4m3fn), not {t.dtype}")
+    return _dev(t, name)
+
+
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: Optional[torch.Tensor] = None,
              lse: Optional[torch.Tensor] = None, scale: float = 0.0, want_lse: bool = True,
              stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
@@ -137,7 +154,7 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: Optional[torc
         lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
     _check("attn_fwd", lib().attn_fwd(
         _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(o, "o"), _ptr_or_null(lse, "lse"),
-        B, H, Sq, Skv, D, _DT[q.dtype], float(scale), _stream(stream)))
+        B, H, Sq, Skv, D, _dt(q, "q"), float(scale), _stream(stream)))
     return o, lse
 
 
@@ -154,7 +171,7 @@ def attn_fwd_chunked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int,
         lse_parts = torch.empty((P, B, H, Sq), dtype=torch.float32, device=q.device)
     _check("attn_fwd_chunked", lib().attn_fwd_chunked(
         _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), int(P), _dev(o_parts, "o_parts"),
-        _dev(lse_parts, "lse_parts"), B, H, Sq, Skv, D, _DT[q.dtype], float(scale),
+        _dev(lse_parts, "lse_parts"), B, H, Sq, Skv, D, _dt(q, "q"), float(scale),
         _stream(stream)))
     return o_parts, lse_parts
 
@@ -170,7 +187,7 @@ def attn_lse_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor,
         lse = torch.empty((B, H, Sq), dtype=torch.float32, device=o_parts.device)
     _check("attn_lse_merge", lib().attn_lse_merge(
         _dev(o_parts, "o_parts"), _dev(lse_parts, "lse_parts"), P, B, H, Sq, D,
-        _DT[o_parts.dtype], _dev(o, "o"), _ptr_or_null(lse, "lse"), _stream(stream)))
+        _dt(o_parts, "o_parts"), _dev(o, "o"), _ptr_or_null(lse, "lse"), _stream(stream)))
     return o, lse
 
 
@@ -186,7 +203,7 @@ def attn_fwd_ring(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int,
         lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
     _check("attn_fwd_ring", lib().attn_fwd_ring(
         _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), P, _dev(o, "o"), _ptr_or_null(lse, "lse"),
-        B, H, Sq, Skv, D, _DT[q.dtype], float(scale), _stream(stream)))
+        B, H, Sq, Skv, D, _dt(q, "q"), float(scale), _stream(stream)))
     return o, lse
 
 
@@ -203,7 +220,7 @@ def attn_fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, vt8: torch.Tensor, P: int, 
     if lse is None and want_lse:
         lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q8.device)
     _check("attn_fwd_fp8", lib().attn_fwd_fp8(
-        _dev(q8, "q"), _dev(k8, "k"), _dev(vt8, "vt"), P, float(q_scale), float(k_scale),
+        _e4m3(q8, "q"), _e4m3(k8, "k"), _e4m3(vt8, "vt"), P, float(q_scale), float(k_scale),
         float(v_scale), _dev(o, "o"), _ptr_or_null(lse, "lse"), B, H, Sq, Skv, D, float(scale),
         _stream(stream)))
     return o, lse
@@ -213,7 +230,7 @@ def cp_absmax(x: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) 
     """max |x| of a bf16/fp16 tensor, as a one-element fp32 device tensor."""
     if out is None:
         out = torch.empty((1,), dtype=torch.float32, device=x.device)
-    _check("cp_absmax", lib().cp_absmax(_dev(x, "x"), x.numel(), _DT[x.dtype], _dev(out, "amax"),
+    _check("cp_absmax", lib().cp_absmax(_dev(x, "x"), x.numel(), _dt(x, "x"), _dev(out, "amax"),
                                         _stream(stream)))
     return out
 
@@ -229,7 +246,7 @@ def cp_quantize_e4m3(x: torch.Tensor, scale: float, transpose: bool = False,
         shape = (*lead, D, S) if transpose else (*lead, S, D)
         out = torch.empty(shape, dtype=torch.uint8, device=x.device)
     _check("cp_quantize_e4m3", lib().cp_quantize_e4m3(
-        _dev(x, "x"), _DT[x.dtype], _dev(out, "y"), BH, S, D, float(scale), int(transpose),
+        _dev(x, "x"), _dt(x, "x"), _dev(out, "y"), BH, S, D, float(scale), int(transpose),
         _stream(stream)))
     return out
 
@@ -246,7 +263,7 @@ def attn_fwd_ulysses(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
         lse = torch.empty((P, B, H // P, Sl * P), dtype=torch.float32, device=q.device)
     _check("attn_fwd_ulysses", lib().attn_fwd_ulysses(
         _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(o, "o"), _ptr_or_null(lse, "lse"),
-        P, B, Sl * P, H, D, _DT[q.dtype], float(scale), _stream(stream)))
+        P, B, Sl * P, H, D, _dt(q, "q"), float(scale), _stream(stream)))
     return o, lse
 
 

@@ -221,3 +221,15 @@ def test_quantize_argument_errors(L_):
     g = L_.cp_absmax
     assert g(A, 12, 0, L, None) == E                        # n must be a multiple of 8
     assert g(A, 16, 0, L + 2, None) == M
+
+
+def test_binding_rejects_wrong_dtypes():
+    """The binding names the argument when a tensor has the wrong element type (checked before
+    the library is called)."""
+    import torch
+    with pytest.raises(ValueError, match="bfloat16 or float16"):
+        cpattn._dt(torch.zeros(4, dtype=torch.float32), "q")
+    with pytest.raises(ValueError, match="e4m3 bytes"):
+        cpattn._e4m3(torch.zeros(4, dtype=torch.bfloat16), "q")
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        cpattn.attn_fwd(*(torch.zeros(1, 1, 16, 64, dtype=torch.bfloat16) for _ in range(3)))
