@@ -557,7 +557,9 @@ def _ulysses_leg(cpattn, dev, stream, iters=5):
 def run_profile_case(args):
     """One kernel only, for an ncu capture: W + K launches on a reduced case that still exceeds
     L2 -- attn: the video shape with --heads heads (default 2: Q/K/V 22.6 MB each, partials
-    181 MB), P=8; merge: the same partials; layout: the Ulysses shape (134 MB each side)."""
+    181 MB), P=8; merge: the same partials; layout: the Ulysses shape (134 MB each side);
+    ulysses: the fused Ulysses attention on the full Ulysses shape ([8][2][2048][32][64] fp16,
+    134 MB per tensor); fp8: the e4m3 attention on the video shape with --heads heads, P=8."""
     from context_math_non_b300 import cpattn
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -571,6 +573,20 @@ def run_profile_case(args):
                 cpattn.attn_fwd_chunked(q, k, v, P_CHUNKS, op, lp)
             else:
                 cpattn.attn_lse_merge(op, lp)
+    elif args.profile == "ulysses":
+        q, k, v = (t.to(dev) for t in draw_qkv(WORKLOADS["ulysses"]))
+        o, lse = cpattn.attn_fwd_ulysses(q, k, v)
+        for _ in range(args.warmup + args.steps):
+            cpattn.attn_fwd_ulysses(q, k, v, o, lse)
+    elif args.profile == "fp8":
+        q, k, v = (t.to(dev) for t in draw_qkv(w, H=H))
+        scales = [cpattn.cp_absmax(t).item() / 448.0 for t in (q, k, v)]
+        q8 = cpattn.cp_quantize_e4m3(q, scales[0])
+        k8 = cpattn.cp_quantize_e4m3(k, scales[1])
+        vt8 = cpattn.cp_quantize_e4m3(v, scales[2], transpose=True)
+        o, lse = cpattn.attn_fwd_fp8(q8, k8, vt8, P_CHUNKS, *scales)
+        for _ in range(args.warmup + args.steps):
+            cpattn.attn_fwd_fp8(q8, k8, vt8, P_CHUNKS, *scales, o=o, lse=lse)
     else:
         wu = WORKLOADS["ulysses"]
         x = draw_qkv(wu)[0].to(dev)
@@ -641,7 +657,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=24)
-    ap.add_argument("--profile", choices=["attn", "merge", "layout"], default=None,
+    ap.add_argument("--profile", choices=["attn", "merge", "layout", "ulysses", "fp8"],
+                    default=None,
                     help="run one kernel on the reduced profiling case (for ncu) and exit")
     ap.add_argument("--heads", type=int, default=None)
     ap.add_argument("--probe", action="store_true",
