@@ -75,50 +75,59 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint4* __restrict__
   }
 }
 
-// Transposed per head: block = one 64 (tokens) x 64 (features) tile of one head.  Loads are
-// 16-byte vectors along the features, stores 16-byte vectors of e4m3 along the tokens.
-constexpr int kT = 64;
+// Transposed per head: block = one 128 (tokens) x 64 (features) tile of one head.  Thread
+// (tq, fo) loads 4 tokens x 8 features (four 16-byte vectors; the 8 threads of a token row
+// cover its 128 bytes) and packs, per feature, its 4 tokens' e4m3 bytes into one 32-bit word.
+// Shared memory holds [64 features][128 tokens] bytes with the 16-byte chunks of feature row r
+// XOR-swizzled by r / 8, so the word stores (one chunk per feature octet) and the 16-byte
+// loads of the read-out are both free of bank conflicts; each output row of 128 tokens is then
+// written as eight 16-byte vectors.
+constexpr int kTT = 128, kTF = 64;
 template <bool BF16>
 __global__ void __launch_bounds__(256) quantize_t_kernel(const uint16_t* __restrict__ in,
                                                          uint8_t* __restrict__ out, int BH, int S,
                                                          int D, float inv_scale) {
-  __shared__ __align__(16) uint8_t tile[kT][kT + 16];   // [feature][token], padded rows
-  const int s0 = blockIdx.x * kT, d0 = blockIdx.y * kT;
+  __shared__ __align__(16) uint32_t tile[kTF * kTT / 4];   // [feature][32 words of 4 tokens]
+  const int s0 = blockIdx.x * kTT, d0 = blockIdx.y * kTF;
+  const int tq = threadIdx.x >> 3, fo = threadIdx.x & 7;     // token quad, feature octet
   for (long long head = blockIdx.z; head < BH; head += gridDim.z) {
-  const uint16_t* src = in + head * S * static_cast<long long>(D);
-  uint8_t* dst = out + head * D * static_cast<long long>(S);
-  __syncthreads();   // the previous head's tile has been read out
-  // 64 tokens x 8 vectors of 8 features: 512 vectors, two per thread
-  for (int v = threadIdx.x; v < kT * (kT / 8); v += 256) {
-    const int sl = v >> 3, dv = (v & 7) * 8;
-    const int s = s0 + sl;
-    float f[8];
-    if (s < S) {
-      unpack8<BF16>(__ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(s) * D +
-                                                        d0 + dv)),
-                    f);
-    } else {
+    const uint16_t* src = in + head * S * static_cast<long long>(D);
+    uint8_t* dst = out + head * D * static_cast<long long>(S);
+    __syncthreads();   // the previous head's tile has been read out
+    float f[4][8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) f[k] = 0.f;
+    for (int r = 0; r < 4; ++r) {
+      const int s = s0 + 4 * tq + r;
+      if (s < S) {
+        unpack8<BF16>(__ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(s) * D +
+                                                          d0 + 8 * fo)),
+                      f[r]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f[r][k] = 0.f;
+      }
     }
 #pragma unroll
-    for (int k = 0; k < 8; k += 4) {
-      const uint32_t q = ptx::pack4_e4m3(f[k] * inv_scale, f[k + 1] * inv_scale,
-                                         f[k + 2] * inv_scale, f[k + 3] * inv_scale);
+    for (int k = 0; k < 8; ++k) {
+      const int row = 8 * fo + k;                       // feature within the tile
+      const int word = tq;                              // tokens 4 tq .. 4 tq + 3
+      const int chunk = (word >> 2) ^ (row >> 3);       // 16-byte chunk, swizzled
+      tile[row * 32 + chunk * 4 + (word & 3)] =
+          ptx::pack4_e4m3(f[0][k] * inv_scale, f[1][k] * inv_scale, f[2][k] * inv_scale,
+                          f[3][k] * inv_scale);
+    }
+    __syncthreads();
+    // 64 features x 8 chunks of 16 tokens: 512 vectors, two per thread
 #pragma unroll
-      for (int b = 0; b < 4; ++b) tile[dv + k + b][sl] = static_cast<uint8_t>(q >> (8 * b));
+    for (int i = 0; i < 2; ++i) {
+      const int v = threadIdx.x + 256 * i;
+      const int row = v >> 3, c = v & 7;
+      const int s = s0 + 16 * c;
+      if (s < S) {   // S is a multiple of 16: a chunk is either fully inside or outside
+        const uint4 r = *reinterpret_cast<const uint4*>(&tile[row * 32 + ((c ^ (row >> 3)) * 4)]);
+        *reinterpret_cast<uint4*>(dst + static_cast<long long>(d0 + row) * S + s) = r;
+      }
     }
-  }
-  __syncthreads();
-  // 64 features x 4 vectors of 16 tokens: 256 vectors, one per thread
-  {
-    const int dl = threadIdx.x >> 2, sv = (threadIdx.x & 3) * 16;
-    const int s = s0 + sv;
-    if (s < S) {   // S is a multiple of 16, so a vector is either fully inside or outside
-      const uint4 r = *reinterpret_cast<const uint4*>(&tile[dl][sv]);
-      *reinterpret_cast<uint4*>(dst + static_cast<long long>(d0 + dl) * S + s) = r;
-    }
-  }
   }
 }
 
@@ -159,7 +168,7 @@ attn_status launch_quantize_e4m3(const void* in, bool bf16, void* out, int BH, i
       quantize_kernel<false><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(in),
                                                        static_cast<uint4*>(out), n16x2, inv_scale);
   } else {
-    const dim3 grid((S + kT - 1) / kT, D / kT, BH < 65535 ? BH : 65535);
+    const dim3 grid((S + kTT - 1) / kTT, D / kTF, BH < 65535 ? BH : 65535);
     if (bf16)
       quantize_t_kernel<true><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(in),
                                                         static_cast<uint8_t*>(out), BH, S, D,
