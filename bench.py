@@ -358,7 +358,9 @@ def _e2e_leg(cpattn, q, k, v, dev, stream, args, flops, world):
     for i in range(max(1, args.warmup)):
         step(i)
     torch.cuda.synchronize(dev)
-    steps = max(2, args.steps // 2)
+    # as many steps as the device-timed loop; the first step's upload and the last step's
+    # download are inside the timed region and not overlapped (pipeline fill and drain)
+    steps = max(2, args.steps)
     if world > 1:
         torch.distributed.barrier()
     a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
