@@ -642,6 +642,19 @@ def run_mma_probe():
         out[label] = round(sms * steps * 2 * 4 * 128 * 128 * D / ms / 1e9, 1)
     ms = rate(128, 4, 32000)
     out["handoff_round_trip_ns"] = round(ms * 1e6 / 4000, 1)
+    # ALU rates of the softmax's instruction mix (ops per ns per SM; per clock = / GHz)
+    alu = {}
+    for mode, label in ((0, "ex2_approx"), (1, "cvt_bf16x2"), (2, "fma_f32x2_pairs"),
+                        (3, "fma_f32")):
+        iters = 4096
+        cpattn.attn_probe_alu(mode, 256)
+        torch.cuda.synchronize()
+        a.record()
+        cpattn.attn_probe_alu(mode, iters)
+        b.record()
+        torch.cuda.synchronize()
+        alu[label] = round(2 * 512 * iters * 8 / (a.elapsed_time(b) * 1e6), 2)
+    out["alu_ops_per_ns_per_sm"] = alu
     out["gemm_128x128x128_ns_at_peak"] = round(2 * 128 ** 3 / (2.26e15 / sms) * 1e9, 1)
     st = cpattn.attn_device_status()
     if st != cpattn.ATTN_OK:

@@ -17,7 +17,7 @@ __all__ = ["CpAttnError", "CpAttnLibraryError", "lib", "attn_fwd", "attn_fwd_chu
            "attn_lse_merge", "attn_fwd_ulysses", "attn_fwd_ring", "attn_fwd_fp8", "cp_absmax",
            "cp_quantize_e4m3", "cp_layout_seq2head",
            "cp_layout_head2seq", "attn_device_status",
-           "attn_watchdog_selftest", "attn_set_max_ctas", "attn_probe_mma",
+           "attn_watchdog_selftest", "attn_set_max_ctas", "attn_probe_mma", "attn_probe_alu",
            "attn_set_kernel_variant", "attn_status_string", "attn_version",
            "LIB_PATH", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
            "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT"]
@@ -74,12 +74,13 @@ def lib() -> ctypes.CDLL:
     L.attn_set_max_ctas.argtypes = [i]
     L.attn_set_kernel_variant.argtypes = [i]
     L.attn_probe_mma.argtypes = [i, i, i, vp]
+    L.attn_probe_alu.argtypes = [i, i, vp]
     L.attn_version.argtypes = []
     for name in ("attn_fwd", "attn_fwd_chunked", "attn_lse_merge", "attn_fwd_ulysses",
                  "attn_fwd_ring", "attn_fwd_fp8", "cp_absmax", "cp_quantize_e4m3",
                  "cp_layout_seq2head", "cp_layout_head2seq",
                  "attn_device_status", "attn_watchdog_selftest", "attn_set_max_ctas",
-                 "attn_version", "attn_probe_mma", "attn_set_kernel_variant"):
+                 "attn_version", "attn_probe_mma", "attn_probe_alu", "attn_set_kernel_variant"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -291,6 +292,10 @@ def attn_probe_mma(n: int, mode: int, iters: int, stream=None):
     """Launch the tensor-core ceiling probe (time it with CUDA events around the call)."""
     _check("attn_probe_mma", lib().attn_probe_mma(int(n), int(mode), int(iters),
                                                    _stream(stream)))
+
+
+def attn_probe_alu(mode: int, iters: int, stream=None):
+    _check("attn_probe_alu", lib().attn_probe_alu(int(mode), int(iters), _stream(stream)))
 
 
 def attn_device_status(stream=None) -> int:

@@ -267,6 +267,11 @@ attn_status attn_probe_mma(int n, int mode, int iters, attn_stream_t stream) {
   return cpattn::launch_mma_probe(n, mode, iters, reinterpret_cast<cudaStream_t>(stream));
 }
 
+attn_status attn_probe_alu(int mode, int iters, attn_stream_t stream) {
+  if (mode < 0 || mode > 3 || iters < 1) return ATTN_ERR_INVALID_ARG;
+  return cpattn::launch_alu_probe(mode, iters, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int attn_set_kernel_variant(int v) { return cpattn::set_attention_variant(v != 0 ? 1 : 0); }
 
 int attn_set_max_ctas(int n) { return g_max_ctas.exchange(n > 0 ? n : 0); }

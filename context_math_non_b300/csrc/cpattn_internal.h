@@ -58,4 +58,6 @@ attn_status read_and_clear_device_status(cudaStream_t stream);
 
 attn_status launch_mma_probe(int n, int mode, int iters, cudaStream_t stream);
 
+attn_status launch_alu_probe(int mode, int iters, cudaStream_t stream);
+
 }  // namespace cpattn

@@ -267,3 +267,65 @@ attn_status launch_mma_probe(int n, int mode, int iters, cudaStream_t stream) {
 }
 
 }  // namespace cpattn
+
+// ----------------------------------------------------------------------------- ALU probes
+// Throughput of the softmax's instruction mix: every thread runs 8 independent dependent chains
+// of one operation; 2 blocks of 512 threads per SM keep every scheduler busy.  Mode 0: MUFU
+// ex2.approx.ftz.f32; 1: cvt.rn.bf16x2.f32; 2: fma.rn.f32x2 (counted as one pair); 3: scalar
+// fma.rn.f32.  The caller times the launch: ops = SMs * 2 * 512 * iters * 8.
+namespace cpattn {
+namespace {
+
+__device__ __forceinline__ uint32_t cvt_bf16x2_probe(float lo, float hi) {
+  uint32_t r;
+  asm volatile("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <int kMode>
+__global__ void __launch_bounds__(512) alu_probe_kernel(int iters) {
+  float x[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) x[i] = 0.1f * (threadIdx.x & 7) + 0.05f * i;
+  uint64_t x2[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) x2[i] = ptx::f2_pack(x[i], x[i] + 0.01f);
+  const uint64_t c2 = ptx::f2_pack(0.999f, 0.998f), d2 = ptx::f2_pack(0.001f, 0.002f);
+  for (int it = 0; it < iters; ++it) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if constexpr (kMode == 0) {
+        x[i] = ptx::ex2(-x[i]);            // 2^-x stays in [0.5, 1] for x in [0, 1]
+      } else if constexpr (kMode == 1) {
+        x[i] = __uint_as_float(cvt_bf16x2_probe(x[i], x[(i + 1) & 7]));
+      } else if constexpr (kMode == 2) {
+        x2[i] = ptx::f2_fma(x2[i], c2, d2);
+      } else {
+        x[i] = fmaf(x[i], 0.999f, 0.001f);
+      }
+    }
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float a, b;
+    ptx::f2_unpack(x2[i], a, b);
+    s += x[i] + a + b;
+  }
+  if (s == 1.2345f) g_probe_status = 99;   // keeps the chains alive; never true in practice
+}
+
+}  // namespace
+
+attn_status launch_alu_probe(int mode, int iters, cudaStream_t stream) {
+  const int sms = device_sm_count();
+  if (sms <= 0) return ATTN_ERR_CUDA;
+  const int grid = 2 * sms;
+  if (mode == 0) alu_probe_kernel<0><<<grid, 512, 0, stream>>>(iters);
+  else if (mode == 1) alu_probe_kernel<1><<<grid, 512, 0, stream>>>(iters);
+  else if (mode == 2) alu_probe_kernel<2><<<grid, 512, 0, stream>>>(iters);
+  else alu_probe_kernel<3><<<grid, 512, 0, stream>>>(iters);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace cpattn

@@ -245,6 +245,15 @@ CPATTN_API int attn_set_max_ctas(int n);
 CPATTN_API attn_status attn_probe_mma(int n, int mode, int iters, attn_stream_t stream);
 
 /*
+ * attn_probe_alu -- throughput probe of the softmax's instruction mix (calibration).
+ *   2 blocks of 512 threads per SM; every thread runs 8 independent dependent chains of one
+ *   operation for `iters` iterations.  mode 0: ex2.approx.ftz.f32 (MUFU); 1: cvt.rn.bf16x2.f32;
+ *   2: fma.rn.f32x2 (one pair per op); 3: fma.rn.f32.  The caller times the launch:
+ *   ops = SMs * 2 * 512 * iters * 8.  ATTN_ERR_INVALID_ARG for other modes or iters < 1.
+ */
+CPATTN_API attn_status attn_probe_alu(int mode, int iters, attn_stream_t stream);
+
+/*
  * attn_set_kernel_variant -- choose the attention kernel for D = 128 (process-wide, affects later
  *   launches): 0 (default) runs the single-CTA kernel; 1 runs it on pairs of SMs (cta_group::2
  *   MMAs, each CTA loading half of every K/V tile -- measured slower on B300, kept for testing

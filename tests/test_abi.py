@@ -233,3 +233,9 @@ def test_binding_rejects_wrong_dtypes():
         cpattn._e4m3(torch.zeros(4, dtype=torch.bfloat16), "q")
     with pytest.raises(ValueError, match="CUDA tensor"):
         cpattn.attn_fwd(*(torch.zeros(1, 1, 16, 64, dtype=torch.bfloat16) for _ in range(3)))
+
+
+def test_alu_probe_argument_errors(L_):
+    assert L_.attn_probe_alu(4, 10, None) == cpattn.ATTN_ERR_INVALID_ARG
+    assert L_.attn_probe_alu(-1, 10, None) == cpattn.ATTN_ERR_INVALID_ARG
+    assert L_.attn_probe_alu(0, 0, None) == cpattn.ATTN_ERR_INVALID_ARG
