@@ -453,24 +453,49 @@ def run_reference(args):
     }
 
 
-def _ring_leg(cpattn, qd, kd, vd, o, lse, dev, stream, flops, step_ms, iters=5):
+def _ring_leg(cpattn, qd, kd, vd, o, lse, dev, stream, flops, step_ms, iters=6):
     """The same video problem through attn_fwd_ring (P = 8 ring steps, merge fused into the
-    kernel: no partial outputs in HBM, no merge launch), against the step above."""
-    cpattn.attn_fwd_ring(qd, kd, vd, P_CHUNKS, o, lse, stream=stream)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(iters)]
-    for a, b in evs:
-        a.record(stream)
+    kernel: no partial outputs in HBM, no merge launch) and through the chunked step + merge,
+    launched alternately so both see the same clocks and power state."""
+    w = WORKLOAD
+    op = torch.empty((P_CHUNKS, w.B, w.H, w.S, w.D), dtype=w.dtype, device=dev)
+    lp = torch.empty((P_CHUNKS, w.B, w.H, w.S), dtype=torch.float32, device=dev)
+
+    def ring():
         cpattn.attn_fwd_ring(qd, kd, vd, P_CHUNKS, o, lse, stream=stream)
-        b.record(stream)
-    torch.cuda.synchronize(dev)
+
+    def chunked():
+        cpattn.attn_fwd_chunked(qd, kd, vd, P_CHUNKS, op, lp, stream=stream)
+        cpattn.attn_lse_merge(op, lp, o, lse, stream=stream)
+
+    ms = _interleaved({"ring": ring, "chunked_plus_merge": chunked}, dev, stream, iters)
     st = cpattn.attn_device_status(stream)
     if st != cpattn.ATTN_OK:
         raise RuntimeError(f"device status after ring leg: {cpattn.attn_status_string(st)}")
-    ms = statistics.median(a.elapsed_time(b) for a, b in evs)
-    return {"attn_fwd_ring_P8": {"median_ms": round(ms, 4),
-                                 "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1),
-                                 "vs_chunked_plus_merge_step_ms": round(step_ms, 4)}}
+    del op, lp
+    return {"attn_fwd_ring_P8": {"median_ms": round(ms["ring"], 4),
+                                 "TFLOP/s": round(flops / (ms["ring"] * 1e-3) / 1e12, 1),
+                                 "chunked_plus_merge_median_ms":
+                                     round(ms["chunked_plus_merge"], 4),
+                                 "order": "launched alternately with the chunked step"}}
+
+
+def _interleaved(fns, dev, stream, iters):
+    """Median CUDA-event time of each callable, the callables launched in turn `iters` times
+    (one warm-up round first), so slow drifts of clock and power affect all alike."""
+    for fn in fns.values():
+        fn()
+    torch.cuda.synchronize(dev)
+    times = {n: [] for n in fns}
+    for _ in range(iters):
+        for n, fn in fns.items():
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            times[n].append(a.elapsed_time(b))
+    return {n: statistics.median(t) for n, t in times.items()}
 
 
 def _fp8_leg(cpattn, qd, kd, vd, o, lse, dev, stream, flops, peaks, iters=5):
@@ -514,7 +539,7 @@ def _fp8_leg(cpattn, qd, kd, vd, o, lse, dev, stream, flops, peaks, iters=5):
                                 "quantize_qkv_ms": round(out["quantize_qkv"], 4)}}
 
 
-def _ulysses_leg(cpattn, dev, stream, iters=5):
+def _ulysses_leg(cpattn, dev, stream, iters=6):
     """Ulysses attention on [8][2][2048][32][64] fp16 (S = 16384, 32 heads): the fused kernel
     (sequence-sharded addressing, no re-layout passes) against the unfused chain of
     seq2head(Q, K, V) -> attention on [16][4][16384][64] -> head2seq(O)."""
@@ -537,18 +562,10 @@ def _ulysses_leg(cpattn, dev, stream, iters=5):
         cpattn.cp_layout_head2seq(oh.view(P, B, H // P, S, D), o, stream=stream)
 
     flops = 4.0 * B * H * S * S * D
-    out = {}
-    for name, fn in (("fused", fused), ("unfused_chain", chain)):
-        fn()
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(iters)]
-        for a, b in evs:
-            a.record(stream)
-            fn()
-            b.record(stream)
-        torch.cuda.synchronize(dev)
-        ms = statistics.median(a.elapsed_time(b) for a, b in evs)
-        out[name] = {"median_ms": round(ms, 4), "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1)}
+    ms = _interleaved({"fused": fused, "unfused_chain": chain}, dev, stream, iters)
+    out = {n: {"median_ms": round(t, 4), "TFLOP/s": round(flops / (t * 1e-3) / 1e12, 1)}
+           for n, t in ms.items()}
+    out["order"] = "launched alternately"
     st = cpattn.attn_device_status(stream)
     if st != cpattn.ATTN_OK:
         raise RuntimeError(f"device status after Ulysses leg: {cpattn.attn_status_string(st)}")
