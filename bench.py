@@ -662,7 +662,8 @@ def run_mma_probe():
     # ALU rates of the softmax's instruction mix (ops per ns per SM; per clock = / GHz)
     alu = {}
     for mode, label in ((0, "ex2_approx"), (1, "cvt_bf16x2"), (2, "fma_f32x2_pairs"),
-                        (3, "fma_f32")):
+                        (3, "fma_f32"), (4, "ex2_approx_bf16x2_pairs"),
+                        (5, "ex2_approx_f16x2_pairs")):
         iters = 4096
         cpattn.attn_probe_alu(mode, 256)
         torch.cuda.synchronize()

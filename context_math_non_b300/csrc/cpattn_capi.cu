@@ -268,7 +268,7 @@ attn_status attn_probe_mma(int n, int mode, int iters, attn_stream_t stream) {
 }
 
 attn_status attn_probe_alu(int mode, int iters, attn_stream_t stream) {
-  if (mode < 0 || mode > 3 || iters < 1) return ATTN_ERR_INVALID_ARG;
+  if (mode < 0 || mode > 5 || iters < 1) return ATTN_ERR_INVALID_ARG;
   return cpattn::launch_alu_probe(mode, iters, reinterpret_cast<cudaStream_t>(stream));
 }
 

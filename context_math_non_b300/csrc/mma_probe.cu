@@ -272,7 +272,9 @@ attn_status launch_mma_probe(int n, int mode, int iters, cudaStream_t stream) {
 // Throughput of the softmax's instruction mix: every thread runs 8 independent dependent chains
 // of one operation; 2 blocks of 512 threads per SM keep every scheduler busy.  Mode 0: MUFU
 // ex2.approx.ftz.f32; 1: cvt.rn.bf16x2.f32; 2: fma.rn.f32x2 (counted as one pair); 3: scalar
-// fma.rn.f32.  The caller times the launch: ops = SMs * 2 * 512 * iters * 8.
+// fma.rn.f32; 4: ex2.approx.ftz.bf16x2 and 5: ex2.approx.f16x2 (one op = two exponentials, plus
+// a sign flip on the integer pipe).  The caller times the launch:
+// ops = SMs * 2 * 512 * iters * 8.
 namespace cpattn {
 namespace {
 
@@ -300,6 +302,14 @@ __global__ void __launch_bounds__(512) alu_probe_kernel(int iters) {
         x[i] = __uint_as_float(cvt_bf16x2_probe(x[i], x[(i + 1) & 7]));
       } else if constexpr (kMode == 2) {
         x2[i] = ptx::f2_fma(x2[i], c2, d2);
+      } else if constexpr (kMode == 4 || kMode == 5) {
+        // two exponentials per op; the sign flip keeps 2^-x in [0.5, 1]
+        uint32_t h = __float_as_uint(x[i]) ^ 0x80008000u;
+        if constexpr (kMode == 4)
+          asm volatile("ex2.approx.ftz.bf16x2 %0, %0;" : "+r"(h));
+        else
+          asm volatile("ex2.approx.f16x2 %0, %0;" : "+r"(h));
+        x[i] = __uint_as_float(h);
       } else {
         x[i] = fmaf(x[i], 0.999f, 0.001f);
       }
@@ -324,7 +334,9 @@ attn_status launch_alu_probe(int mode, int iters, cudaStream_t stream) {
   if (mode == 0) alu_probe_kernel<0><<<grid, 512, 0, stream>>>(iters);
   else if (mode == 1) alu_probe_kernel<1><<<grid, 512, 0, stream>>>(iters);
   else if (mode == 2) alu_probe_kernel<2><<<grid, 512, 0, stream>>>(iters);
-  else alu_probe_kernel<3><<<grid, 512, 0, stream>>>(iters);
+  else if (mode == 3) alu_probe_kernel<3><<<grid, 512, 0, stream>>>(iters);
+  else if (mode == 4) alu_probe_kernel<4><<<grid, 512, 0, stream>>>(iters);
+  else alu_probe_kernel<5><<<grid, 512, 0, stream>>>(iters);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -248,7 +248,8 @@ CPATTN_API attn_status attn_probe_mma(int n, int mode, int iters, attn_stream_t 
  * attn_probe_alu -- throughput probe of the softmax's instruction mix (calibration).
  *   2 blocks of 512 threads per SM; every thread runs 8 independent dependent chains of one
  *   operation for `iters` iterations.  mode 0: ex2.approx.ftz.f32 (MUFU); 1: cvt.rn.bf16x2.f32;
- *   2: fma.rn.f32x2 (one pair per op); 3: fma.rn.f32.  The caller times the launch:
+ *   2: fma.rn.f32x2 (one pair per op); 3: fma.rn.f32; 4: ex2.approx.ftz.bf16x2 and
+ *   5: ex2.approx.f16x2 (two exponentials per op).  The caller times the launch:
  *   ops = SMs * 2 * 512 * iters * 8.  ATTN_ERR_INVALID_ARG for other modes or iters < 1.
  */
 CPATTN_API attn_status attn_probe_alu(int mode, int iters, attn_stream_t stream);

@@ -236,6 +236,6 @@ def test_binding_rejects_wrong_dtypes():
 
 
 def test_alu_probe_argument_errors(L_):
-    assert L_.attn_probe_alu(4, 10, None) == cpattn.ATTN_ERR_INVALID_ARG
+    assert L_.attn_probe_alu(6, 10, None) == cpattn.ATTN_ERR_INVALID_ARG
     assert L_.attn_probe_alu(-1, 10, None) == cpattn.ATTN_ERR_INVALID_ARG
     assert L_.attn_probe_alu(0, 0, None) == cpattn.ATTN_ERR_INVALID_ARG
