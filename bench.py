@@ -3,13 +3,15 @@
 One step = the ring-emulation hot path on the video-DiT workload (B=1, H=16, S=44,160, D=128,
 bf16): attn_fwd_chunked over P=8 KV chunks, then attn_lse_merge of the eight partials.  The
 metric is attention TFLOP/s = 4*B*H*Sq*Skv*D per step / step time.  Extra legs report the
-attention kernel alone against the tensor-core roofline, the merge and Ulysses layout kernels in
+attention kernel alone against the tensor-core roofline (measured sustained and burst peaks, and
+the clock-derived nominal at the SM clock sampled during the timed region), the merge and Ulysses
+layout kernels in
 GB/s against HBM, an end-to-end number through the same API with host buffers, and the CPU
 oracle timed on a bounded sample.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
                     [--no-cpu-baseline] [--no-e2e]
-    python bench.py --profile attn|merge|layout    # one kernel, reduced case, for ncu
+    python bench.py --profile attn|merge|layout|ulysses|fp8   # one kernel, reduced case, for ncu
     python bench.py --probe                         # tensor-core calibration probes
 
 Prints one JSON line (rank 0).  With torchrun each rank runs an independent replica of the same
@@ -260,6 +262,15 @@ def run_native(args, rank, world, local_rank):
     legs.update(_ring_leg(cpattn, qd, kd, vd, o, lse, dev, stream, flops, ms_per_step))
     legs.update(_fp8_leg(cpattn, qd, kd, vd, o, lse, dev, stream, flops, peaks))
     clk = clocks.summary()
+    # clock-derived nominal: SMs x 8192 dense bf16 flop per clock (one M128 N256 K16 MMA per
+    # 64 clocks) at the median SM clock seen during the timed region, and at the maximum clock
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    if clk is not None:
+        nominal = sms * 8192 * clk["sm_mhz"] * 1e6 / 1e12
+        roofline["clock_nominal"] = {
+            "peak_at_median_clock": round(nominal, 1),
+            "frac": round(achieved / nominal, 4),
+            "peak_at_max_clock": round(sms * 8192 * clk["sm_max_mhz"] * 1e6 / 1e12, 1)}
 
     e2e = None
     if not args.no_e2e:
@@ -421,6 +432,7 @@ def cpu_baseline(q, k, v, budget_s: float = 15.0):
     flops = 4.0 * w.B * w.H * rows * w.S * w.D
     return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": _blas_threads(),
             "kind": "oracle", "seconds": round(dt, 2),
+            "extrapolated_full_seconds": round(dt * w.S / rows, 1),
             "sample": f"first {rows} query rows of each of the {w.H} heads (of {w.S}), full KV, "
                       f"P=8 chunks + merge, float64 numpy"}
 
