@@ -19,7 +19,8 @@
 //   warps 4-7  softmax for query tile 1
 //   warp  8    TMA producer: Q tiles once per unit, then K_j / V_j through a ring of stages
 //   warp  9    TMEM allocation and MMA issue: the whole warp runs the loop (waits voted across
-//              the warp) and one elected lane issues, so the operands stay warp-uniform
+//              the warp) and one elected lane issues by predication, so the operands stay
+//              warp-uniform
 //   warp  10   with separate P (D = 64): issues the O += P V GEMMs while warp 9 issues S
 //   warps 10-11 otherwise idle (they complete the third warpgroup, which releases registers to
 //              the softmax warpgroups with setmaxnreg)
@@ -482,12 +483,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp || (C::SEP_P && warp == kMmaWarp + 1)) {
     // ------------------------------------------------------------------ MMA issuers
     // The whole warp runs its loop with identical control flow (every wait is voted across
-    // the warp); one elected lane issues each MMA and commit.  With separate P the S = Q K^T
+    // the warp); one lane issues every MMA and commit.  With separate P the S = Q K^T
     // GEMMs (this warp) and the O += P V GEMMs (the next warp) touch disjoint tensor-memory
     // columns and are ordered only through the softmax hand-offs, so two warps issue them:
     // each issuing warp is a serial chain of waits and issues, and splitting it halves the
     // chain per KV step.
     {
+      // The issuing lane, chosen once (the warp stays converged through the whole loop), or an
+      // elect.sync per instruction: one choice per schedule, by measurement (the single elect
+      // is ≈ 3-4 % faster with one issuing warp, ≈ 1.5 % slower with the two of separate P).
+      constexpr bool kElectOnce = !C::SEP_P;
+      const uint32_t lead = kElectOnce ? ptx::elect_leader() : 0u;
+      auto mma_ss = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+        if constexpr (kElectOnce) ptx::mma_ss_lead(lead, d, a, b, id, acc);
+        else ptx::mma_ss_elect(d, a, b, id, acc);
+      };
+      auto mma_ts = [&](uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
+        if constexpr (kElectOnce) ptx::mma_ts_lead(lead, d, a, b, id, acc);
+        else ptx::mma_ts_elect(d, a, b, id, acc);
+      };
+      auto mma_ss_f8 = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+        if constexpr (kElectOnce) ptx::mma_ss_f8_lead(lead, d, a, b, id, acc);
+        else ptx::mma_ss_f8_elect(d, a, b, id, acc);
+      };
+      auto mma_ts_f8 = [&](uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
+        if constexpr (kElectOnce) ptx::mma_ts_f8_lead(lead, d, a, b, id, acc);
+        else ptx::mma_ts_f8_elect(d, a, b, id, acc);
+      };
+      auto commit = [&](uint64_t* bar) {
+        if constexpr (kElectOnce) ptx::mma_commit_lead(lead, bar);
+        else ptx::mma_commit_elect(bar);
+      };
       // e4m3 (kF8): format code 0 in both operand fields and a K-major B (V^T) for P*V
       constexpr uint32_t kIdescS = ptx::idesc_f16(kF8 ? false : BF16, false, kBM, kBN);
       constexpr uint32_t kIdescPV = ptx::idesc_f16(kF8 ? false : BF16, !kF8, kBM, D);
@@ -504,14 +530,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           // K = 32 one-byte elements per MMA: 32-byte steps inside the 128-byte rows
 #pragma unroll
           for (int ks = 0; ks < D / 32; ++ks)
-            ptx::mma_ss_f8_elect(d_s, da + 2 * ks, db + 2 * ks, kIdescS, ks > 0);
+            mma_ss_f8(d_s, da + 2 * ks, db + 2 * ks, kIdescS, ks > 0);
         } else {
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             // descriptor start-address field counts 16-byte units; no carry can leave it
             const uint64_t off =
                 static_cast<uint64_t>(((ks >> 2) * kHalfBytes + (ks & 3) * 32) >> 4);
-            ptx::mma_ss_elect(d_s, da + off, db + off, kIdescS, ks > 0);
+            mma_ss(d_s, da + off, db + off, kIdescS, ks > 0);
           }
         }
       };
@@ -524,13 +550,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t dvt = ptx::smem_desc_sw128(b0, 16, 1024);
 #pragma unroll
           for (int ks = 0; ks < kBN / 32; ++ks)
-            ptx::mma_ts_f8_elect(d_o, a_p + ks * 8, dvt + 2 * ks, kIdescPV,
+            mma_ts_f8(d_o, a_p + ks * 8, dvt + 2 * ks, kIdescPV,
                                  (acc || ks > 0) ? 1u : 0u);
         } else {
           const uint64_t dv = ptx::smem_desc_sw128(b0, kHalfBytes, 1024);
 #pragma unroll
           for (int ks = 0; ks < kBN / 16; ++ks) {
-            ptx::mma_ts_elect(d_o, a_p + ks * 8, dv + static_cast<uint64_t>(ks * 128), kIdescPV,
+            mma_ts(d_o, a_p + ks * 8, dv + static_cast<uint64_t>(ks * 128), kIdescPV,
                               (acc || ks > 0) ? 1u : 0u);
           }
         }
@@ -580,24 +606,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (j == 0 && !(ok = vote_wait(&q_full[t], it & 1))) break;
                 ptx::tc_fence_after();
                 issue_s(t, st);
-                ptx::mma_commit_elect(&s_full[t]);
-                if (j == w.n - 1) ptx::mma_commit_elect(&q_empty[t]);
+                commit(&s_full[t]);
+                if (j == w.n - 1) commit(&q_empty[t]);
               } else {
                 if (!(ok = vote_wait(&p_full[t], pph[t]))) break;
                 pph[t] ^= 1;
                 if (j == 0 && it > 0 && !(ok = vote_wait(&o_empty[t], (it - 1) & 1))) break;
                 ptx::tc_fence_after();
                 issue_pv(t, st, j > 0);
-                ptx::mma_commit_elect(&pv_done[t]);
-                if (j == w.n - 1) ptx::mma_commit_elect(&o_full[t]);
+                commit(&pv_done[t]);
+                if (j == w.n - 1) commit(&o_full[t]);
               }
             }
             if (!ok) break;
-            ptx::mma_commit_elect(&kv_empty[st]);
+            commit(&kv_empty[st]);
           }
         }
         // All MMAs this warp issued complete before TMEM is released.
-        ptx::mma_commit_elect(&mma_drain[s_role ? 0 : 1]);
+        commit(&mma_drain[s_role ? 0 : 1]);
         drain_wait(&mma_drain[s_role ? 0 : 1], 0, lim);
       } else {
       for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
@@ -610,11 +636,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           ptx::tc_fence_after();
           issue_s(t, sk);
-          ptx::mma_commit_elect(&s_full[t]);
-          if (w.n == 1) ptx::mma_commit_elect(&q_empty[t]);
+          commit(&s_full[t]);
+          if (w.n == 1) commit(&q_empty[t]);
         }
         if (!ok) break;
-        ptx::mma_commit_elect(&kv_empty[sk]);
+        commit(&kv_empty[sk]);
 
         for (int j = 1; ok && j <= w.n; ++j) {
           if (!(ok = wait_kv(sv))) break;
@@ -631,21 +657,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ptx::tc_fence_after();
             issue_pv(t, sv, j > 1);
-            if (t == kQT - 1) ptx::mma_commit_elect(&kv_empty[sv]);
+            if (t == kQT - 1) commit(&kv_empty[sv]);
             if (j == w.n) {
-              ptx::mma_commit_elect(&o_full[t]);
+              commit(&o_full[t]);
             } else {
               if (t == 0 && !(ok = wait_kv(sk))) break;
               issue_s(t, sk);
-              ptx::mma_commit_elect(&s_full[t]);
-              if (j == w.n - 1) ptx::mma_commit_elect(&q_empty[t]);
-              if (t == kQT - 1) ptx::mma_commit_elect(&kv_empty[sk]);
+              commit(&s_full[t]);
+              if (j == w.n - 1) commit(&q_empty[t]);
+              if (t == kQT - 1) commit(&kv_empty[sk]);
             }
           }
         }
       }
       // All MMAs this warp issued complete before TMEM is released.
-      ptx::mma_commit_elect(&mma_drain[0]);
+      commit(&mma_drain[0]);
       drain_wait(&mma_drain[0], 0, lim);
       }
     }
