@@ -490,13 +490,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // chain per KV step.
     {
       // The issuing lane, chosen once (the warp stays converged through the whole loop), or an
-      // elect.sync per instruction: one choice per schedule, by measurement (the single elect
-      // is ≈ 3-4 % faster with one issuing warp, ≈ 1.5 % slower with the two of separate P).
-      constexpr bool kElectOnce = !C::SEP_P;
-      const uint32_t lead = kElectOnce ? ptx::elect_leader() : 0u;
+      // elect.sync per instruction: chosen per schedule and GEMM by measurement.  With one
+      // issuing warp the single elect is ≈ 3-4 % faster; with the two warps of separate P it
+      // gains ≈ 1 % for the S GEMMs and loses for the P*V GEMMs and the commits.
+      constexpr bool kElectOnce = !C::SEP_P;   // for the P*V GEMMs and the commits
+      const uint32_t lead = ptx::elect_leader();
       auto mma_ss = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
-        if constexpr (kElectOnce) ptx::mma_ss_lead(lead, d, a, b, id, acc);
-        else ptx::mma_ss_elect(d, a, b, id, acc);
+        ptx::mma_ss_lead(lead, d, a, b, id, acc);
       };
       auto mma_ts = [&](uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
         if constexpr (kElectOnce) ptx::mma_ts_lead(lead, d, a, b, id, acc);
