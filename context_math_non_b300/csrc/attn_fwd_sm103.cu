@@ -502,14 +502,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kElectOnce) ptx::mma_ts_lead(lead, d, a, b, id, acc);
         else ptx::mma_ts_elect(d, a, b, id, acc);
       };
-      auto mma_ss_f8 = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
-        if constexpr (kElectOnce) ptx::mma_ss_f8_lead(lead, d, a, b, id, acc);
-        else ptx::mma_ss_f8_elect(d, a, b, id, acc);
-      };
-      auto mma_ts_f8 = [&](uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
-        if constexpr (kElectOnce) ptx::mma_ts_f8_lead(lead, d, a, b, id, acc);
-        else ptx::mma_ts_f8_elect(d, a, b, id, acc);
-      };
       auto commit = [&](uint64_t* bar) {
         if constexpr (kElectOnce) ptx::mma_commit_lead(lead, bar);
         else ptx::mma_commit_elect(bar);
@@ -527,10 +519,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t da = ptx::smem_desc_sw128(a0, 16, 1024);
         const uint64_t db = ptx::smem_desc_sw128(b0, 16, 1024);
         if constexpr (kF8) {
-          // K = 32 one-byte elements per MMA: 32-byte steps inside the 128-byte rows
-#pragma unroll
-          for (int ks = 0; ks < D / 32; ++ks)
-            mma_ss_f8(d_s, da + 2 * ks, db + 2 * ks, kIdescS, ks > 0);
+          // K = 32 one-byte elements per MMA: four 32-byte steps inside the 128-byte rows, one
+          // assembly block (measured +2.5 % over one MMA per block for this schedule)
+          static_assert(D == 128 && !C::SEP_P, "e4m3 path: D = 128, one issuing warp");
+          ptx::gemm_ss_f8_d128(lead, d_s, da, db, kIdescS);
         } else {
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
@@ -548,10 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kF8) {
           // A = P (e4m3, 8 columns per 32 keys), B = the V^T tile, K-major over the keys
           const uint64_t dvt = ptx::smem_desc_sw128(b0, 16, 1024);
-#pragma unroll
-          for (int ks = 0; ks < kBN / 32; ++ks)
-            mma_ts_f8(d_o, a_p + ks * 8, dvt + 2 * ks, kIdescPV,
-                                 (acc || ks > 0) ? 1u : 0u);
+          ptx::gemm_ts_f8_n128(lead, d_o, a_p, dvt, kIdescPV, acc ? 1u : 0u);
         } else {
           const uint64_t dv = ptx::smem_desc_sw128(b0, kHalfBytes, 1024);
 #pragma unroll

@@ -204,22 +204,6 @@ __device__ __forceinline__ void mma_ts_lead(uint32_t lead, uint32_t d_tmem, uint
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(lead));
 }
-__device__ __forceinline__ void mma_ss_f8_lead(uint32_t lead, uint32_t d_tmem, uint64_t a_desc,
-                                               uint64_t b_desc, uint32_t idesc,
-                                               uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 e, %5, 0;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(lead));
-}
-__device__ __forceinline__ void mma_ts_f8_lead(uint32_t lead, uint32_t d_tmem, uint32_t a_tmem,
-                                               uint64_t b_desc, uint32_t idesc,
-                                               uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 e, %5, 0;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(lead));
-}
 __device__ __forceinline__ void mma_commit_lead(uint32_t lead, uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\tsetp.ne.b32 e, %1, 0;\n\t"
@@ -250,22 +234,76 @@ __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
       : "memory");
 }
 
-// kind::f8f6f4 forms (8-bit operands, here e4m3 x e4m3 -> f32): K = 32 per instruction, the
+// kind::f8f6f4 GEMMs (8-bit operands, here e4m3 x e4m3 -> f32): K = 32 per instruction, the
 // instruction descriptor is the kind::f16 layout with format code 0 (E4M3) for A and B.  Both
-// operands are K-major in this library (the 8-bit B operand is always given K-major).
-__device__ __forceinline__ void mma_ss_f8_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                                uint32_t idesc, uint32_t accumulate) {
+// operands are K-major in this library (the 8-bit B operand is always given K-major).  Each
+// helper issues one whole 128 x 128 x 128 GEMM (four MMAs) from lane `lead` of a converged warp
+// in one assembly block: the predicates are set once and the K steps advance the descriptors'
+// start-address field (16-byte units, low bits of the low word) by 32 bytes with 32-bit adds,
+// which cannot carry out of the field for shared-memory addresses below 256 KB.
+//   gemm_ss_f8_d128: D[128 x 128] = A[128 x 128] * B[128 x 128]^T, both from shared memory,
+//                    D overwritten.
+__device__ __forceinline__ void gemm_ss_f8_d128(uint32_t lead, uint32_t d_tmem, uint64_t a_desc,
+                                                uint64_t b_desc, uint32_t idesc) {
   asm volatile(
-      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+      "{\n\t"
+      ".reg .pred e, p0, p1;\n\t"
+      ".reg .b32 alo, ahi, blo, bhi, ta, tb;\n\t"
+      ".reg .b64 ad, bd;\n\t"
+      "setp.ne.b32 e, %3, 0;\n\t"
+      "setp.ne.b32 p0, %3, %3;\n\t"
+      "setp.eq.b32 p1, %3, %3;\n\t"
+      "mov.b64 {alo, ahi}, %1;\n\t"
+      "mov.b64 {blo, bhi}, %2;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %4, p0;\n\t"
+      "add.u32 ta, alo, 2;\n\t"
+      "add.u32 tb, blo, 2;\n\t"
+      "mov.b64 ad, {ta, ahi};\n\t"
+      "mov.b64 bd, {tb, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ad, bd, %4, p1;\n\t"
+      "add.u32 ta, alo, 4;\n\t"
+      "add.u32 tb, blo, 4;\n\t"
+      "mov.b64 ad, {ta, ahi};\n\t"
+      "mov.b64 bd, {tb, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ad, bd, %4, p1;\n\t"
+      "add.u32 ta, alo, 6;\n\t"
+      "add.u32 tb, blo, 6;\n\t"
+      "mov.b64 ad, {ta, ahi};\n\t"
+      "mov.b64 bd, {tb, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ad, bd, %4, p1;\n\t"
+      "}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(lead), "r"(idesc));
 }
-__device__ __forceinline__ void mma_ts_f8_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                uint32_t idesc, uint32_t accumulate) {
+//   gemm_ts_f8_n128: D[128 x 128] (+)= A[128 x 128] * B, A from tensor memory (4 e4m3 per
+//                    column, 8 columns per K step), B [128 x 128] K-major from shared memory;
+//                    the first MMA accumulates only when `accumulate` is non-zero.
+__device__ __forceinline__ void gemm_ts_f8_n128(uint32_t lead, uint32_t d_tmem, uint32_t a_tmem,
+                                                uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
+      "{\n\t"
+      ".reg .pred e, p0, p1;\n\t"
+      ".reg .b32 blo, bhi, ta, tb;\n\t"
+      ".reg .b64 bd;\n\t"
+      "setp.ne.b32 e, %3, 0;\n\t"
+      "setp.ne.b32 p0, %5, 0;\n\t"
+      "setp.eq.b32 p1, %3, %3;\n\t"
+      "mov.b64 {blo, bhi}, %2;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %4, p0;\n\t"
+      "add.u32 ta, %1, 8;\n\t"
+      "add.u32 tb, blo, 2;\n\t"
+      "mov.b64 bd, {tb, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [ta], bd, %4, p1;\n\t"
+      "add.u32 ta, %1, 16;\n\t"
+      "add.u32 tb, blo, 4;\n\t"
+      "mov.b64 bd, {tb, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [ta], bd, %4, p1;\n\t"
+      "add.u32 ta, %1, 24;\n\t"
+      "add.u32 tb, blo, 6;\n\t"
+      "mov.b64 bd, {tb, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [ta], bd, %4, p1;\n\t"
+      "}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(lead), "r"(idesc), "r"(accumulate));
 }
 
 // CTA-pair forms (cta_group::2): allocation, dealloc and relinquish are issued by one warp in
