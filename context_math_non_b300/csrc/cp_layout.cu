@@ -8,9 +8,12 @@
 //   head-sharded Y[g][b][j][t][d]  (rank g holds heads g*H/P + j, all S tokens)
 //   Y[g][b][j][p*S/P + s][d] = X[p][b][s][g*H/P + j][d].
 //
-// Threads walk one side's index space linearly in 16-byte vectors; the matching vector on the
-// other side is part of a run of D*elem_bytes contiguous bytes, so both sides are accessed in
-// whole 16-byte vectors and in runs of at least one (token, head) row.
+// Rows of a power-of-two number of 16-byte vectors (every D here) go through a tiled kernel whose
+// blocks each own one (rank, head) pair and a run of tokens, so the index arithmetic is a few
+// multiply-adds per vector.  Other row sizes use a general kernel whose threads walk one side's
+// index space linearly; the matching vector on the other side is part of a run of D*elem_bytes
+// contiguous bytes, so both sides are accessed in whole 16-byte vectors and in runs of at least
+// one (token, head) row.
 
 #include <cuda_runtime.h>
 
@@ -87,6 +90,47 @@ __global__ void __launch_bounds__(kLayoutThreads)
   }
 }
 
+// Tiled form for rows of a power-of-two number of vectors (vpr = 2^vpr_log2 <= 256): block
+// (p, sb) x (g, b, j) moves tokens s in [sb*TT, (sb+1)*TT) of rank p for head j of rank g, batch b,
+// TT = kUnroll * 256 / vpr.  All coordinates come from the block index, so a vector costs a few
+// multiply-adds instead of the general kernel's chain of divisions; the head-sharded side of a
+// block is one contiguous run of TT rows, the sequence-sharded side TT rows H*vpr vectors apart.
+template <bool kSeq2Head>
+__global__ void __launch_bounds__(kLayoutThreads)
+    layout_tile_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, int B, int Hl, int S,
+                       int Sl, int H, int vpr_log2, int nsb) {
+  const int gbj = blockIdx.y;                   // (g * B + b) * Hl + j
+  const int j = gbj % Hl;
+  const int gb = gbj / Hl;
+  const int b = gb % B;
+  const int g = gb / B;
+  const int p = blockIdx.x / nsb;
+  const int sb = blockIdx.x - p * nsb;
+  const int rows = kLayoutThreads >> vpr_log2;  // token rows per pass of the block
+  const int x = threadIdx.x & ((1 << vpr_log2) - 1);
+  const int rl = threadIdx.x >> vpr_log2;
+  // row indices of token s = 0 of this (rank, head) on both sides
+  const long long seq_row0 = static_cast<long long>(p * B + b) * Sl * H + g * Hl + j;
+  const long long head_row0 = static_cast<long long>(gbj) * S + static_cast<long long>(p) * Sl;
+  uint4 v[kUnroll];
+  long long dst[kUnroll];
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    const int s = (sb * kUnroll + u) * rows + rl;
+    if (s < Sl) {
+      const long long seq_i = ((seq_row0 + static_cast<long long>(s) * H) << vpr_log2) + x;
+      const long long head_i = ((head_row0 + s) << vpr_log2) + x;
+      v[u] = __ldcs(in + (kSeq2Head ? seq_i : head_i));
+      dst[u] = kSeq2Head ? head_i : seq_i;
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    const int s = (sb * kUnroll + u) * rows + rl;
+    if (s < Sl) __stcs(out + dst[u], v[u]);
+  }
+}
+
 template <typename Idx>
 cudaError_t launch_layout_typed(const void* in, void* out, long long total, int B, int Hl, int S,
                                 int Sl, int H, int vpr, bool seq2head, cudaStream_t stream) {
@@ -118,6 +162,23 @@ attn_status launch_layout(const void* in, void* out, int P, int B, int S, int H,
   const int Sl = S / P;
   const long long total = static_cast<long long>(P) * B * Hl * S * vpr;
   cudaError_t e;
+  int vpr_log2 = 0;
+  while ((1 << vpr_log2) < vpr) ++vpr_log2;
+  const long long heads = static_cast<long long>(P) * B * Hl;
+  if ((1 << vpr_log2) == vpr && vpr <= kLayoutThreads && heads <= 65535) {
+    const int tokens_per_block = kUnroll * (kLayoutThreads / vpr);
+    const int nsb = (Sl + tokens_per_block - 1) / tokens_per_block;
+    const dim3 grid(static_cast<unsigned>(static_cast<long long>(P) * nsb),
+                    static_cast<unsigned>(heads));
+    if (seq2head)
+      layout_tile_kernel<true><<<grid, kLayoutThreads, 0, stream>>>(
+          static_cast<const uint4*>(in), static_cast<uint4*>(out), B, Hl, S, Sl, H, vpr_log2, nsb);
+    else
+      layout_tile_kernel<false><<<grid, kLayoutThreads, 0, stream>>>(
+          static_cast<const uint4*>(in), static_cast<uint4*>(out), B, Hl, S, Sl, H, vpr_log2, nsb);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  }
   // 32-bit index arithmetic when every index (all bounded by total) and the loop counter, which
   // can step past total by one grid stride, stay far below 2^32.
   if (total < (1ll << 31))
