@@ -28,6 +28,8 @@ def bits(t: torch.Tensor) -> np.ndarray:
     (8, 2, 64, 16, 16, torch.float32),     # 4-byte elements
     (1, 2, 10, 3, 8, torch.float16),       # P = 1 is a pure transpose [B][S][H] -> [B][H][S]
     (3, 1, 9, 6, 24, torch.float16),       # non-power-of-two P and D
+    (2, 1, 30, 2, 512, torch.float16),     # 64 vectors per row: 16-token runs, ragged last run
+    (2, 2, 1030, 4, 4, torch.float32),     # one vector per row: a 515-token rank in one 1024-token run
 ])
 def test_layout_small_bit_exact(P, B, S, H, D, dtype):
     g = torch.Generator().manual_seed(P * 100 + S)
