@@ -428,6 +428,53 @@ def test_fp8_p_rounding_bound():
     pin_p8_bound(oracle.fp8_p_rounding_bound)
 
 
+def _fp8_inputs(seed, lead=(2,), Sq=7, Skv=19, D=16, spread=2.0):
+    """e4m3 bytes of seeded normal draws (torch's float8_e4m3fn conversion: never a NaN code)."""
+    g = torch.Generator().manual_seed(seed)
+    mk = lambda n, s: (torch.randn(lead + (n, D), generator=g) * s).to(
+        torch.float8_e4m3fn).view(torch.uint8).numpy()
+    return mk(Sq, spread), mk(Skv, spread), mk(Skv, 1.0)
+
+
+def pin_attention_fp8(fn):
+    """FP8 attention is exact attention on the real values the bytes stand for, byte x scale
+    (page section on quantisation: FP8 for attention layers).  Pinned without the oracle's own
+    decoder: torch decodes the bytes, scales them and runs its float64 SDPA; then the scale
+    relations that any correct placement of the three scales obeys."""
+    qs, ks, vs = 0.37, 0.052, 1.9
+    for seed, sc in ((1, None), (2, 0.21)):
+        q8, k8, v8 = _fp8_inputs(seed)
+        dec = lambda b, s: torch.from_numpy(b).view(torch.float8_e4m3fn).to(torch.float64) * s
+        q, k, v = dec(q8, qs), dec(k8, ks), dec(v8, vs)
+        scale = 1.0 / math.sqrt(q.shape[-1]) if sc is None else sc
+        ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, scale=scale)
+        lse_ref = torch.logsumexp((q @ k.transpose(-1, -2)) * scale, dim=-1)
+        o, lse = fn(q8, k8, v8, qs, ks, vs, scale=sc)
+        np.testing.assert_allclose(o, ref.numpy(), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lse, lse_ref.numpy(), rtol=1e-12, atol=1e-12)
+    q8, k8, v8 = _fp8_inputs(3)
+    o, lse = fn(q8, k8, v8, qs, ks, vs)
+    # V's scale multiplies O and nothing else (exact: a power of two)
+    o2, lse2 = fn(q8, k8, v8, qs, ks, 2.0 * vs)
+    np.testing.assert_array_equal(o2, 2.0 * o)
+    np.testing.assert_array_equal(lse2, lse)
+    # only the product of Q's and K's scales enters the logits
+    o3, lse3 = fn(q8, k8, v8, 3.0 * qs, ks / 3.0, vs)
+    np.testing.assert_allclose(o3, o, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse3, lse, rtol=1e-12, atol=1e-13)
+    # doubling Q's scale is attention on doubled real queries (sharper softmax, not a scaled O)
+    o4, lse4 = fn(q8, k8, v8, 2.0 * qs, ks, vs)
+    dec = lambda b, s: torch.from_numpy(b).view(torch.float8_e4m3fn).to(torch.float64).numpy() * s
+    o5, lse5 = oracle.attention(dec(q8, 2.0 * qs), dec(k8, ks), dec(v8, vs))
+    np.testing.assert_allclose(o4, o5, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse4, lse5, rtol=1e-12, atol=1e-12)
+    assert np.abs(o4 - o).max() > 1e-3
+
+
+def test_attention_fp8_scales():
+    pin_attention_fp8(oracle.attention_fp8)
+
+
 def test_raw_fp32_and_rounded_inputs_agree_to_bf16_precision():
     """tiny workload: the fp32 draw and its bf16 rounding give outputs within bf16 input error."""
     from context_math_non_b300.inputs import WORKLOADS, draw_qkv
@@ -565,6 +612,17 @@ def _mutants():
         o, lse = oracle.ulysses_attention(q, k, v, P)
         return o, np.ascontiguousarray(lse.transpose(1, 0, 2, 3))
 
+    def fp8_no_v_scale(q8, k8, v8, qs, ks, vs, scale=None):
+        return base.attention_fp8(q8, k8, v8, qs, ks, 1.0, scale)
+
+    def fp8_q_scale_twice(q8, k8, v8, qs, ks, vs, scale=None):
+        return base.attention_fp8(q8, k8, v8, qs * qs, ks, vs, scale)
+
+    def fp8_scales_outside_softmax(q8, k8, v8, qs, ks, vs, scale=None):
+        # the logits see the raw bytes; the Q and K scales multiply the output instead
+        o, lse = base.attention_fp8(q8, k8, v8, 1.0, 1.0, vs, scale)
+        return o * qs * ks, lse
+
     return [
         ("attention: no scale", lambda: pin_torch_sdpa(no_scale)),
         ("attention: transposed V", lambda: pin_bruteforce(transposed_v)),
@@ -585,6 +643,9 @@ def _mutants():
         ("e4m3: rounds toward zero", lambda: pin_e4m3_round(round_toward_zero)),
         ("e4m3: P bound too tight", lambda: pin_p8_bound(p8_bound_too_tight)),
         ("ulysses: batch-major LSE", lambda: pin_ulysses(ulysses_lse_batch_major)),
+        ("fp8: V scale dropped", lambda: pin_attention_fp8(fp8_no_v_scale)),
+        ("fp8: Q scale applied twice", lambda: pin_attention_fp8(fp8_q_scale_twice)),
+        ("fp8: scales outside the softmax", lambda: pin_attention_fp8(fp8_scales_outside_softmax)),
     ]
 
 
