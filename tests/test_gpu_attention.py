@@ -9,7 +9,8 @@ import torch
 import oracle
 from context_math_non_b300 import cpattn
 from context_math_non_b300.inputs import WORKLOADS, draw_qkv
-from parity import assert_attention_close, oracle_rows, sample_rows, to_np
+from parity import (assert_attention_close, merge_reference, oracle_rows, sample_rows,
+                    to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -32,7 +33,8 @@ def run_full_and_chunked(q, k, v, P, what):
     op_ref, lp_ref = oracle.attention_chunked(q, k, v, P)
     assert_attention_close(o, lse, o_ref, lse_ref, f"{what} attn_fwd")
     assert_attention_close(op, lp, op_ref, lp_ref, f"{what} chunked P={P}")
-    assert_attention_close(om, lm, o_ref, lse_ref, f"{what} chunked P={P} + merge")
+    om_ref, lm_ref = merge_reference(op_ref, lp_ref, q.dtype)
+    assert_attention_close(om, lm, om_ref, lm_ref, f"{what} chunked P={P} + merge")
     return o, lse
 
 
@@ -99,6 +101,23 @@ def test_large_logits_no_overflow():
     assert lse.min().item() > 80.0
 
 
+def test_sharp_softmax_large_logits():
+    """Q x 12: logits with standard deviation 12 (peaks near 50), so one or two keys carry most of
+    each row's weight and O is close to single rows of V (|O| up to 4); the running max jumps by
+    tens between tiles and chunks.  Here the 16-bit rounding of P (relative 2^-9, with P up to
+    2^8 under the lazy rescale) meets |O| ~ |v|, the hardest case for the bf16 tolerance."""
+    q, k, v = rand_qkv(1, 2, 384, 700, 128, torch.bfloat16, seed=5, q_scale=12.0)
+    o, lse = run_full_and_chunked(q, k, v, 3, "sharp softmax")
+    assert o.float().abs().max().item() > 3.0 and lse.max().item() > 30.0
+    orr, lrr = cpattn.attn_fwd_ring(q.cuda(), k.cuda(), v.cuda(), 3)
+    o_ref, lse_ref = oracle.attention(q, k, v)
+    assert_attention_close(orr, lrr, o_ref, lse_ref, "sharp softmax ring P=3")
+    qh, kh, vh = (t.to(torch.float16) for t in (q, k, v))
+    oh, lh = cpattn.attn_fwd(qh.cuda(), kh.cuda(), vh.cuda())
+    o_ref, lse_ref = oracle.attention(qh, kh, vh)
+    assert_attention_close(oh, lh, o_ref, lse_ref, "sharp softmax fp16")
+
+
 def test_many_units_per_cta():
     """A grid capped at 2 CTAs (one SM pair) walks every unit of the problem: exercises every
     barrier phase wrap, on both kernels."""
@@ -163,7 +182,7 @@ def test_image_workload_sampled(image_inputs, P):
     op_ref, lp_ref = oracle_rows(q, k, v, rows, P)
     assert_attention_close(op[:, :, :, rows].cpu(), lp[:, :, :, rows].cpu(), op_ref, lp_ref,
                            f"image chunked P={P}")
-    o_ref, lse_ref = oracle.lse_merge(op_ref, lp_ref)
+    o_ref, lse_ref = merge_reference(op_ref, lp_ref)
     assert_attention_close(om[:, :, rows].cpu(), lm[:, :, rows].cpu(), o_ref, lse_ref,
                            f"image P={P} merged")
 
