@@ -47,7 +47,8 @@ CONFIG = {
     "workload": "video-DiT long sequence: B=1 H=16 S=44160 D=128 bf16 N(0,1), non-causal, "
                 "KV split into P=8 chunks (per-chunk O + LSE), then LSE merge",
     "B": 1, "H": 16, "S": 44160, "D": 128, "P": P_CHUNKS,
-    "l2": "no flush: every input is larger than L2 (Q/K/V 181 MB each, partials 1.45 GB)",
+    "l2": "step: every input is larger than L2 (Q/K/V 181 MB each, partials 1.45 GB); the "
+          "merge and layout legs are timed apart with an L2 flush / rotated buffers",
     "parallelism": "replicas",
 }
 ATTN_SOURCES = ["context_math_non_b300/csrc/attn_fwd_sm103.cu",
@@ -242,21 +243,21 @@ def run_native(args, rank, world, local_rank):
     roofline = {
         "kernel": "attn_fwd_kernel<128,bf16> (attn_fwd_chunked, P=8)",
         "bound": "tensor", "achieved": round(achieved, 2),
-        "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
-        "frac": round(achieved / peaks["bf16_sustained"], 4),
-        "peak_note": f"{peaks['source']} sustained dense bf16 (kernel timed inside a long step); "
-                     f"frac of {peaks['source']} burst peak {peaks['bf16']}: "
-                     f"{achieved / peaks['bf16']:.4f}",
+        "peak": peaks["bf16"], "unit": "TFLOP/s",
+        "frac": round(achieved / peaks["bf16"], 4),
+        "peak_note": f"{peaks['source']} burst dense bf16 (the timed region lasts well under a "
+                     f"second); of {peaks['source']} sustained {peaks['bf16_sustained']} (taken "
+                     f"over seconds at a lower clock): {achieved / peaks['bf16_sustained']:.4f}",
         "avg_launch_ms": round(attn_avg, 4),
         "traffic": _traffic(),
         "algorithmic_flops_per_launch": flops,
     }
     legs = {
-        "lse_merge": {"avg_ms": round(merge_avg, 4), "bytes": merge_bytes,
-                      "GB/s": round(merge_bytes / (merge_avg * 1e-3) / 1e9, 1),
-                      "frac_of_hbm": round(merge_bytes / (merge_avg * 1e-3) / 1e9 /
-                                           peaks["hbm_gbs"], 4)},
+        "lse_merge_in_step": {"avg_ms": round(merge_avg, 4), "bytes": merge_bytes,
+                              "note": "inside the timed step, right after the chunked kernel "
+                                      "wrote the partials (part of them may still be in L2)"},
     }
+    legs.update(_merge_leg(cpattn, op, lp, o, lse, dev, stream, peaks, merge_bytes))
     legs.update(_layout_leg(cpattn, dev, stream, peaks))
     legs.update(_ulysses_leg(cpattn, dev, stream))
     legs.update(_ring_leg(cpattn, qd, kd, vd, o, lse, dev, stream, flops, ms_per_step))
@@ -293,6 +294,31 @@ def run_native(args, rank, world, local_rank):
     return line
 
 
+NOMINAL_HBM_GBS = 8000.0   # the nominal B300 HBM3e bandwidth the merge and layout are held to
+
+
+def _merge_leg(cpattn, op, lp, o, lse, dev, stream, peaks, nbytes, iters=10):
+    """attn_lse_merge alone on the video partials (1653 MB per call): before every timed launch a
+    512 MB buffer is written, which evicts the 126 MB L2, so every partial comes from DRAM."""
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    cpattn.attn_lse_merge(op, lp, o, lse, stream=stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(iters)]
+    for i in range(iters):
+        flush.fill_(i & 0xFF)
+        evs[i][0].record(stream)
+        cpattn.attn_lse_merge(op, lp, o, lse, stream=stream)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del flush
+    return {"lse_merge": {"median_ms": round(ms, 4), "bytes": nbytes, "GB/s": round(gbs, 1),
+                          "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                          "frac_of_nominal_8TBs": round(gbs / NOMINAL_HBM_GBS, 4),
+                          "l2": "flushed (512 MB write) before every timed launch"}}
+
+
 def _layout_leg(cpattn, dev, stream, peaks, iters=10):
     """Ulysses seq2head on the Ulysses workload shape ([8][2][2048][32][64] fp16, 134 MB):
     the buffers are rotated over 4 sets (1.07 GB) so no iteration reads from L2."""
@@ -317,7 +343,9 @@ def _layout_leg(cpattn, dev, stream, peaks, iters=10):
     del sets
     return {"cp_layout_seq2head": {"median_ms": round(ms, 4), "bytes": 2 * nbytes,
                                    "GB/s": round(gbs, 1),
-                                   "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}}
+                                   "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                                   "frac_of_nominal_8TBs": round(gbs / NOMINAL_HBM_GBS, 4),
+                                   "l2": "4 rotated buffer sets (1.07 GB)"}}
 
 
 def _e2e_leg(cpattn, q, k, v, dev, stream, args, flops, world):

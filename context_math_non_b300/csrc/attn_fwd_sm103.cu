@@ -1188,21 +1188,40 @@ bool make_map(CUtensorMap* map, const void* base, bool bf16, int D, int S, int B
   return r == CUDA_SUCCESS;
 }
 
+// One-time set-up of a kernel on the current device: the dynamic shared-memory limit above 48 KB
+// is a per-device attribute, so it is set once for every device the process launches on, and the
+// kernel's register count is checked against the register split.  Thread-safe.
+constexpr int kMaxDevices = 64;
+struct KernelSetup {
+  std::once_flag once[kMaxDevices];
+  cudaError_t err[kMaxDevices] = {};
+};
+
+template <typename Kernel>
+cudaError_t setup_kernel(KernelSetup& s, Kernel kern, int smem_bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::call_once(s.once[dev], [&] {
+    cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         smem_bytes);
+    cudaFuncAttributes fa;
+    if (r == cudaSuccess) r = cudaFuncGetAttributes(&fa, kern);
+    // see the register split: setmaxnreg needs exactly the launch register count
+    if (r == cudaSuccess && fa.numRegs != kLaunchRegs) r = cudaErrorInvalidKernelImage;
+    s.err[dev] = r;
+  });
+  return s.err[dev];
+}
+
 template <bool BF16>
 cudaError_t launch_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                         const Params& p, int grid, cudaStream_t stream) {
   auto kern = attn_fwd_pair_kernel<BF16>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  static int regs = -1;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
-    cudaFuncAttributes fa;
-    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, kern);
-    if (attr_err == cudaSuccess) regs = fa.numRegs;
-  });
-  if (attr_err != cudaSuccess) return attr_err;
-  if (regs != kLaunchRegs) return cudaErrorInvalidKernelImage;   // see the register split
+  static KernelSetup setup;
+  const cudaError_t e = setup_kernel(setup, kern, kPairSmem);
+  if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, kPairSmem, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
@@ -1211,18 +1230,9 @@ template <int D, bool BF16, bool kSeq = false, bool kRing = false, bool kF8 = fa
 cudaError_t launch_typed(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const Params& p, int grid, cudaStream_t stream) {
   auto kern = attn_fwd_kernel<D, BF16, kSeq, kRing, kF8>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  static int regs = -1;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    Cfg<D, kF8>::SMEM);
-    cudaFuncAttributes fa;
-    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, kern);
-    if (attr_err == cudaSuccess) regs = fa.numRegs;
-  });
-  if (attr_err != cudaSuccess) return attr_err;
-  if (regs != kLaunchRegs) return cudaErrorInvalidKernelImage;   // see the register split
+  static KernelSetup setup;
+  const cudaError_t e = setup_kernel(setup, kern, Cfg<D, kF8>::SMEM);
+  if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, Cfg<D, kF8>::SMEM, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
