@@ -3,7 +3,7 @@ exactly when the stored value is the rounding of the reference, and grows with t
 import numpy as np
 import torch
 
-from parity import merge_reference, round_to, storage_distance
+from parity import partial_storage_allowance, round_to, storage_distance
 
 
 def test_rounded_reference_has_zero_distance():
@@ -31,11 +31,15 @@ def test_distance_counts_what_lies_beyond_half_a_spacing():
     np.testing.assert_allclose(storage_distance(r + ulp, r, dt), ulp / 2, rtol=1e-12)
 
 
-def test_merge_reference_rounds_partials_only():
+def test_partial_storage_allowance_bounds_the_merge_of_rounded_partials():
+    """Merging partials rounded to bf16 moves the merged value by no more than the allowance."""
     rng = np.random.default_rng(5)
-    op = rng.standard_normal((3, 4, 16))
-    lp = rng.standard_normal((3, 4)) * 5
-    om, lm = merge_reference(op, lp, torch.bfloat16)
-    w = np.exp(np.float32(lp).astype(np.float64) - lp.max(0))
-    want = (w[..., None] * round_to(op, torch.bfloat16)).sum(0) / w.sum(0)[..., None]
-    np.testing.assert_allclose(om, want, rtol=1e-12, atol=1e-14)
+    op = rng.standard_normal((3, 400, 16)) * 3
+    lp = rng.standard_normal((3, 400)) * 2
+    w = np.exp(lp - lp.max(0))
+    exact = (w[..., None] * op).sum(0) / w.sum(0)[..., None]
+    stored = round_to(op, torch.bfloat16)
+    merged = (w[..., None] * stored).sum(0) / w.sum(0)[..., None]
+    allow = partial_storage_allowance(stored, lp, torch.bfloat16)
+    assert (np.abs(merged - exact) <= allow * (1 + 1e-9)).all()
+    assert (np.abs(merged - exact) > 0.5 * allow).any()
