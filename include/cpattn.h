@@ -17,9 +17,12 @@
  *    the launch.  Argument errors are detected on the host before anything is launched, and then
  *    nothing is written.  A failed launch returns ATTN_ERR_CUDA.
  *  - Zero-sized batch / head / query / sequence extents are accepted and launch nothing.
- *  - The calls are thread-safe and may run concurrently on different streams.  The only
- *    device-side state is one status word written by the attention kernels' watchdog (see
- *    attn_device_status).
+ *  - The compute calls are thread-safe and may run concurrently on different streams and
+ *    devices (the one-time kernel set-up is done per device).  The only device-side state is
+ *    one status word per device, written by the attention kernels' watchdog and shared by every
+ *    stream and call on that device (see attn_device_status).  attn_set_max_ctas and
+ *    attn_set_kernel_variant are process-wide test and measurement switches: a launch on
+ *    another thread sees either the old or the new setting.
  *  - 16-bit types are IEEE fp16 or bfloat16; LSE values are fp32 natural logarithms.
  */
 #ifndef CPATTN_H
