@@ -102,13 +102,13 @@ def _src_hash() -> str:
 
 
 def _traffic():
-    """DRAM bytes per attention launch from the committed ncu summary, if it was taken on the
-    current kernel source (else None)."""
+    """DRAM bytes (read + write) of one full-size attention launch, from the committed ncu
+    capture of exactly that launch, if it was taken on the current kernel source (else None)."""
     try:
         with open(os.path.join(ROOT, "profiles", "attn_fwd_traffic.json")) as f:
             d = json.load(f)
         if d.get("kernel_source_sha") == _src_hash():
-            return d["bytes_per_launch_full_size"]
+            return d["dram_bytes_read"] + d["dram_bytes_write"]
     except (OSError, KeyError, ValueError):
         pass
     return None
@@ -262,6 +262,7 @@ def run_native(args, rank, world, local_rank):
     legs.update(_ulysses_leg(cpattn, dev, stream))
     legs.update(_ring_leg(cpattn, qd, kd, vd, o, lse, dev, stream, flops, ms_per_step))
     legs.update(_fp8_leg(cpattn, qd, kd, vd, o, lse, dev, stream, flops, peaks))
+    legs.update(_image_leg(cpattn, dev, stream))
     clk = clocks.summary()
     # clock-derived nominal: SMs x 8192 dense bf16 flop per clock (one M128 N256 K16 MMA per
     # 64 clocks) at the median SM clock seen during the timed region, and at the maximum clock
@@ -518,6 +519,37 @@ def _ring_leg(cpattn, qd, kd, vd, o, lse, dev, stream, flops, step_ms, iters=6):
                                  "chunked_plus_merge_median_ms":
                                      round(ms["chunked_plus_merge"], 4),
                                  "order": "launched alternately with the chunked step"}}
+
+
+def _image_leg(cpattn, dev, stream, iters=15):
+    """The image-DiT shape (B=1 H=24 S=4608 D=128 bf16) with KV in P = 8 chunks of 576 keys
+    (4.5 tiles each): the chunked kernel alone, chunked + merge, and the ring path with the merge
+    on chip, against plain attention (P = 1), launched alternately."""
+    w = WORKLOADS["image"]
+    q, k, v = (t.to(dev) for t in draw_qkv(w))
+    P = 8
+    op = torch.empty((P, w.B, w.H, w.S, w.D), dtype=w.dtype, device=dev)
+    lp = torch.empty((P, w.B, w.H, w.S), dtype=torch.float32, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+    fns = {
+        "plain_P1": lambda: cpattn.attn_fwd(q, k, v, o, lse, stream=stream),
+        "chunked_P8": lambda: cpattn.attn_fwd_chunked(q, k, v, P, op, lp, stream=stream),
+        "chunked_P8_plus_merge": lambda: (cpattn.attn_fwd_chunked(q, k, v, P, op, lp,
+                                                                  stream=stream),
+                                          cpattn.attn_lse_merge(op, lp, o, lse, stream=stream)),
+        "ring_P8": lambda: cpattn.attn_fwd_ring(q, k, v, P, o, lse, stream=stream),
+    }
+    ms = _interleaved(fns, dev, stream, iters)
+    st = cpattn.attn_device_status(stream)
+    if st != cpattn.ATTN_OK:
+        raise RuntimeError(f"device status after image leg: {cpattn.attn_status_string(st)}")
+    flops = w.attention_flops()
+    out = {n: {"median_ms": round(t, 4), "TFLOP/s": round(flops / (t * 1e-3) / 1e12, 1)}
+           for n, t in ms.items()}
+    out["order"] = "launched alternately; inputs 28 MB per tensor (L2-resident across launches)"
+    del q, k, v, op, lp, o, lse
+    return {"image_P8": out}
 
 
 def _interleaved(fns, dev, stream, iters):

@@ -76,6 +76,11 @@ constexpr int kLoaderWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Schedules that run a unit's epilogue after the next unit's first tile (see the softmax loop).
+constexpr bool kDeferEpilogueF8 = true;
+constexpr bool kDeferEpilogue16 = false;
+// Output rows are written with 32-byte stores when the output is 32-byte aligned.
+constexpr bool kStore32 = true;
 
 // kF8: e4m3 operands (one byte per element), so a 128-row tile of D = 128 is one 128-byte-wide
 // swizzled box of 16 KB, like a 16-bit tile of D = 64.
@@ -92,6 +97,7 @@ struct Cfg {
   // softmax of S(j) runs (separate-P schedule).  D = 128 writes P over the first half of S.
   static constexpr bool SEP_P = (D == 64 && !kF8);
   static constexpr uint32_t P_COL0 = SEP_P ? 384 : S_COL0, P_COL1 = SEP_P ? 448 : S_COL1;
+  static constexpr bool DEFER_EPILOGUE = kF8 ? kDeferEpilogueF8 : kDeferEpilogue16;
 };
 
 struct Params {
@@ -100,6 +106,7 @@ struct Params {
   int kv_q, kv_r;    // Skv = kv_q * P + kv_r
   float scale_log2;  // softmax scale * log2(e) (times the Q and K scales for e4m3 inputs)
   float o_scale;     // output multiplier: 1, or the V scale for e4m3 inputs
+  int o_align32;     // o is 32-byte aligned: rows are written in whole 32-byte sectors
   void* o;           // [P][BH][Sq][D]  (sequence-sharded layout: see SeqLayout)
   float* lse;        // [P][BH][Sq] or null
   unsigned long long limit_ns;
@@ -701,6 +708,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
 
+    // ---------------------------------------------------------------- epilogue
+    // Output of unit w: normalised O row and LSE.  With DEFER_EPILOGUE it runs after the next
+    // unit's first tile has been handed to the MMA warp, so the wait for the unit's last P*V
+    // and the stores overlap the next unit's GEMMs instead of delaying its first softmax (a
+    // unit's first tile never touches O: it is only overwritten by that tile's P*V, which waits
+    // for o_empty).
+    auto epilogue = [&](const Unit& w, float m, float l) {
+      ok = __all_sync(0xffffffffu,
+                      ptx::mbar_wait(&o_full[t], oph, abort_flag, &g_attn_status, lim));
+      if (!ok) return;
+      oph ^= 1;
+      ptx::tc_fence_after();
+      const int q_row = w.qb * (kQT * kBM) + t * kBM + row;
+      const bool valid = q_row < p.Sq;
+      const float inv_l = p.o_scale / l;
+      const long long prow = static_cast<long long>(kRing ? 0 : w.c) * p.BH + w.bh;
+      uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
+                       out_row_offset<kSeq, D>(prow, w.bh, valid ? q_row : 0, p);
+      // The whole O row goes to registers first, so the accumulator is released (o_empty)
+      // before the normalisation and the global stores: the next output's first P*V, which
+      // overwrites O, waits only for the tensor-memory reads.
+      uint32_t orr[D];
+      tmem_ld_cols<D>(o_addr, orr);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&o_empty[t]);
+      if (valid && p.o_align32) {
+        // 32-byte stores: each writes a whole sector of the row (a thread owns one row)
+#pragma unroll
+        for (int v = 0; v < D / 16; ++v) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            pk[c] = ptx::pack2<BF16>(__uint_as_float(orr[16 * v + 2 * c]) * inv_l,
+                                     __uint_as_float(orr[16 * v + 2 * c + 1]) * inv_l);
+          ptx::st_global_v8(orow + 16 * v, pk);
+        }
+      } else if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+        for (int v = 0; v < D / 8; ++v) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            pk[c] = ptx::pack2<BF16>(__uint_as_float(orr[8 * v + 2 * c]) * inv_l,
+                                     __uint_as_float(orr[8 * v + 2 * c + 1]) * inv_l);
+          dst[v] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+      if (valid && p.lse != nullptr)
+        p.lse[prow * p.Sq + q_row] = (m + __log2f(l)) * 0.69314718055994530942f;
+    };
+    bool pending = false;   // DEFER_EPILOGUE: the previous unit's epilogue has not run yet
+    Unit w_prev{};
+    float m_prev = 0.f, l_prev = 1.f;
+
     for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
       const Unit w = kRing ? decode_ring_unit(u, p) : decode_unit(u, p);
       float m = -INFINITY;   // running max of scaled logits, log2 units
@@ -749,45 +812,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&p_full[t]);
+        if (C::DEFER_EPILOGUE && j == 0 && pending) {
+          pending = false;
+          epilogue(w_prev, m_prev, l_prev);
+          if (!ok) break;
+        }
       }
       if (!ok) break;
-
-      // ---------------------------------------------------------------- epilogue
-      ok = __all_sync(0xffffffffu,
-                      ptx::mbar_wait(&o_full[t], oph, abort_flag, &g_attn_status, lim));
-      if (!ok) break;
-      oph ^= 1;
-      ptx::tc_fence_after();
-      const int q_row = w.qb * (kQT * kBM) + t * kBM + row;
-      const bool valid = q_row < p.Sq;
-      const float inv_l = p.o_scale / l;
-      const long long prow = static_cast<long long>(kRing ? 0 : w.c) * p.BH + w.bh;
-      uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
-                       out_row_offset<kSeq, D>(prow, w.bh, valid ? q_row : 0, p);
-      // The whole O row goes to registers first, so the accumulator is released (o_empty)
-      // before the normalisation and the global stores: the next output's first P*V, which
-      // overwrites O, waits only for the tensor-memory reads.
-      uint32_t orr[D];
-      tmem_ld_cols<D>(o_addr, orr);
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&o_empty[t]);
-      if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(orow);
-#pragma unroll
-        for (int v = 0; v < D / 8; ++v) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            pk[c] = ptx::pack2<BF16>(__uint_as_float(orr[8 * v + 2 * c]) * inv_l,
-                                     __uint_as_float(orr[8 * v + 2 * c + 1]) * inv_l);
-          dst[v] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
-        if (p.lse != nullptr)
-          p.lse[prow * p.Sq + q_row] = (m + __log2f(l)) * 0.69314718055994530942f;
+      if constexpr (C::DEFER_EPILOGUE) {
+        pending = true;
+        w_prev = w;
+        m_prev = m;
+        l_prev = l;
+      } else {
+        epilogue(w, m, l);
       }
     }
+    if (C::DEFER_EPILOGUE && ok && pending) epilogue(w_prev, m_prev, l_prev);
   }
+
 
   ptx::tc_fence_before();
   __syncthreads();
@@ -1282,6 +1325,7 @@ attn_status launch_attention(const void* q, const void* k, const void* v, void* 
   p.scale_log2 = scale * 1.4426950408889634f;
   p.o_scale = 1.f;
   p.o = o;
+  p.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0 && kStore32 ? 1 : 0;
   p.lse = lse;
   p.limit_ns = limit_ns;
   cudaError_t e;
@@ -1360,6 +1404,7 @@ attn_status launch_attention_ulysses(const void* q, const void* k, const void* v
   p.scale_log2 = scale * 1.4426950408889634f;
   p.o_scale = 1.f;
   p.o = o;
+  p.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0 && kStore32 ? 1 : 0;
   p.lse = lse;
   p.limit_ns = limit_ns;
   p.sq_R = R;
@@ -1424,6 +1469,7 @@ attn_status launch_attention_fp8(const void* q, const void* k, const void* vt, v
   p.scale_log2 = scale * q_scale * k_scale * 1.4426950408889634f;
   p.o_scale = v_scale;
   p.o = o;
+  p.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0 && kStore32 ? 1 : 0;
   p.lse = lse;
   p.limit_ns = limit_ns;
   const int grid = p.num_units < sms ? p.num_units : sms;

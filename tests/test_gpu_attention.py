@@ -145,20 +145,27 @@ def test_deterministic():
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
-def test_outputs_stay_in_bounds():
-    """Canary regions around o_parts / lse_parts are untouched (ragged Sq = 1000)."""
-    B, H, Sq, Skv, D, P = 1, 2, 1000, 600, 128, 3
+@pytest.mark.parametrize("D", [128, 64])
+@pytest.mark.parametrize("shift", [0, 8])
+def test_outputs_stay_in_bounds(D, shift):
+    """Canary regions around o_parts / lse_parts are untouched (ragged Sq = 1000).  shift = 8
+    elements puts the output 16 bytes past a 32-byte boundary: rows are then written with
+    16-byte stores instead of 32-byte ones, and both paths must give the same bytes."""
+    B, H, Sq, Skv, P = 1, 2, 1000, 600, 3
     q, k, v = (t.cuda() for t in rand_qkv(B, H, Sq, Skv, D, torch.bfloat16, seed=9))
     n_o, n_l, pad = P * B * H * Sq * D, P * B * H * Sq, 4096
     obuf = torch.full((n_o + 2 * pad,), 7.0, dtype=torch.bfloat16, device="cuda")
     lbuf = torch.full((n_l + 2 * pad,), -3.0, dtype=torch.float32, device="cuda")
-    op = obuf[pad:pad + n_o].view(P, B, H, Sq, D)
+    op = obuf[pad + shift:pad + shift + n_o].view(P, B, H, Sq, D)
     lp = lbuf[pad:pad + n_l].view(P, B, H, Sq)
+    assert (op.data_ptr() % 32 == 0) == (shift == 0) and op.data_ptr() % 16 == 0
     cpattn.attn_fwd_chunked(q, k, v, P, op, lp)
     torch.cuda.synchronize()
-    assert (obuf[:pad] == 7.0).all() and (obuf[pad + n_o:] == 7.0).all()
+    assert (obuf[:pad + shift] == 7.0).all() and (obuf[pad + shift + n_o:] == 7.0).all()
     assert (lbuf[:pad] == -3.0).all() and (lbuf[pad + n_l:] == -3.0).all()
     assert torch.isfinite(op.float()).all() and torch.isfinite(lp).all()
+    ref_o, ref_l = cpattn.attn_fwd_chunked(q, k, v, P)      # fresh, 32-byte aligned outputs
+    assert torch.equal(op, ref_o) and torch.equal(lp, ref_l)
 
 
 # ----------------------------------------------------------------------------- full sizes
