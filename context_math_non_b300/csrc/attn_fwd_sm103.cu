@@ -81,6 +81,10 @@ constexpr bool kDeferEpilogueF8 = true;
 constexpr bool kDeferEpilogue16 = false;
 // Output rows are written with 32-byte stores when the output is 32-byte aligned.
 constexpr bool kStore32 = true;
+// 16-bit plain-layout kernels stage their output rows in shared memory and write them with TMA
+// stores, 32 rows per warp (the e4m3 kernel measured slower with it and stores directly).
+constexpr bool kStageStore = true;
+constexpr int kStageWarpBytes = 32 * 128;   // 32 rows x one 64-column half of 16-bit O
 
 // kF8: e4m3 operands (one byte per element), so a 128-row tile of D = 128 is one 128-byte-wide
 // swizzled box of 16 KB, like a 16-bit tile of D = 64.
@@ -88,10 +92,13 @@ template <int D, bool kF8 = false>
 struct Cfg {
   static constexpr int NH = kF8 ? 1 : D / 64;             // 128-byte-wide boxes per row
   static constexpr int TILE = NH * kHalfBytes;            // bytes of one 128-row tile
-  static constexpr int STAGES = (TILE == kHalfBytes) ? 8 : 5;   // K/V ring depth
+  static constexpr int STAGES = (TILE == kHalfBytes) ? 8 : 4;   // K/V ring depth
   static constexpr int NBARS = 2 * STAGES + 10 * kQT + 2;
+  // output staging: one region per softmax warp (kStageStore)
+  static constexpr bool STAGE_OUT = kStageStore && !kF8;
+  static constexpr int OUT_STAGE = STAGE_OUT ? kQT * 4 * kStageWarpBytes : 0;
   static constexpr int SMEM = 1024 /*alignment slack*/ + kQT * TILE + STAGES * TILE +
-                              NBARS * 8 + 16;
+                              OUT_STAGE + NBARS * 8 + 16;
   static constexpr uint32_t S_COL0 = 0, S_COL1 = 128, O_COL0 = 256, O_COL1 = 256 + D;
   // D = 64 leaves 128 columns free: P gets its own columns, so S(j+1) can be computed while the
   // softmax of S(j) runs (separate-P schedule).  D = 128 writes P over the first half of S.
@@ -373,14 +380,16 @@ template <int D, bool BF16, bool kSeq, bool kRing, bool kF8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const Params p) {
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_o, const Params p) {
   using C = Cfg<D, kF8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
   uint8_t* sKV = smem + kQT * C::TILE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + C::STAGES * C::TILE);
+  uint8_t* sOut = sKV + C::STAGES * C::TILE;   // 1024-byte aligned (tiles are 16 KB multiples)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + C::OUT_STAGE);
   uint64_t* kv_full = bars;
   uint64_t* kv_empty = bars + C::STAGES;
   uint64_t* q_full = bars + 2 * C::STAGES;
@@ -734,7 +743,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&o_empty[t]);
-      if (valid && p.o_align32) {
+      if constexpr (C::STAGE_OUT && !kSeq) {
+        // The warp's 32 rows go through its shared-memory region, one 64-column half at a time
+        // (128-byte swizzled rows: conflict-free 16-byte writes), and leave as one TMA store per
+        // half: whole, coalesced lines; rows past Sq are clipped by the tensor map.
+        uint8_t* stg = sOut + warp * kStageWarpBytes;
+        const uint32_t stg_row = ptx::smem_u32(stg) + lane * 128;
+        const int row0 = w.qb * (kQT * kBM) + t * kBM + wq * 32;
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+          if (lane == 0) ptx::bulk_wait_read_all();   // the region's previous store has read it
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              pk[i] = ptx::pack2<BF16>(__uint_as_float(orr[64 * h + 8 * c + 2 * i]) * inv_l,
+                                       __uint_as_float(orr[64 * h + 8 * c + 2 * i + 1]) * inv_l);
+            ptx::st_shared_v4(stg_row + ((c ^ (lane & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && row0 < p.Sq) {   // a box that starts inside the tensor
+            ptx::tma_store_3d(&tm_o, stg, 64 * h, row0, static_cast<int>(prow));
+            ptx::bulk_commit();
+          }
+        }
+      } else if (valid && p.o_align32) {
         // 32-byte stores: each writes a whole sector of the row (a thread owns one row)
 #pragma unroll
         for (int v = 0; v < D / 16; ++v) {
@@ -829,6 +865,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (C::DEFER_EPILOGUE && ok && pending) epilogue(w_prev, m_prev, l_prev);
+    // this warp's output stores finish before the CTA (and its shared memory) goes away
+    if (C::STAGE_OUT && !kSeq && lane == 0) ptx::bulk_wait_all();
   }
 
 
@@ -1269,14 +1307,16 @@ cudaError_t launch_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
   return cudaGetLastError();
 }
 
+// mo: the output as [rows][Sq][D] 16-bit, box 64 columns x 32 rows (the staged TMA stores of the
+// plain layout; not read by the sequence-sharded kernels).
 template <int D, bool BF16, bool kSeq = false, bool kRing = false, bool kF8 = false>
 cudaError_t launch_typed(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                         const Params& p, int grid, cudaStream_t stream) {
+                         const CUtensorMap& mo, const Params& p, int grid, cudaStream_t stream) {
   auto kern = attn_fwd_kernel<D, BF16, kSeq, kRing, kF8>;
   static KernelSetup setup;
   const cudaError_t e = setup_kernel(setup, kern, Cfg<D, kF8>::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, Cfg<D, kF8>::SMEM, stream>>>(mq, mk, mv, p);
+  kern<<<grid, kThreads, Cfg<D, kF8>::SMEM, stream>>>(mq, mk, mv, mo, p);
   return cudaGetLastError();
 }
 
@@ -1307,9 +1347,10 @@ attn_status launch_attention(const void* q, const void* k, const void* v, void* 
   // D = 128 runs on CTA pairs (needs at least one pair of SMs); D = 64 on single CTAs.
   const bool pair = !ring && D == 128 && g_variant.load() == 1 && sms >= 2;
   const int rows_per_unit = pair ? 4 * kBM : kQT * kBM;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!make_map(&mq, q, bf16, D, Sq, BH) || !make_map(&mk, k, bf16, D, Skv, BH, pair ? 64 : 128) ||
-      !make_map(&mv, v, bf16, D, Skv, BH))
+      !make_map(&mv, v, bf16, D, Skv, BH) ||
+      !make_map(&mo, o, bf16, D, Sq, ring ? BH : P * BH, 32))
     return ATTN_ERR_CUDA;
   Params p;
   p.Sq = Sq;
@@ -1337,17 +1378,17 @@ attn_status launch_attention(const void* q, const void* k, const void* v, void* 
     const int grid = p.num_units < sms ? p.num_units : sms;
     if (ring) {
       if (D == 128)
-        e = bf16 ? launch_typed<128, true, false, true>(mq, mk, mv, p, grid, stream)
-                 : launch_typed<128, false, false, true>(mq, mk, mv, p, grid, stream);
+        e = bf16 ? launch_typed<128, true, false, true>(mq, mk, mv, mo, p, grid, stream)
+                 : launch_typed<128, false, false, true>(mq, mk, mv, mo, p, grid, stream);
       else
-        e = bf16 ? launch_typed<64, true, false, true>(mq, mk, mv, p, grid, stream)
-                 : launch_typed<64, false, false, true>(mq, mk, mv, p, grid, stream);
+        e = bf16 ? launch_typed<64, true, false, true>(mq, mk, mv, mo, p, grid, stream)
+                 : launch_typed<64, false, false, true>(mq, mk, mv, mo, p, grid, stream);
     } else if (D == 128) {
-      e = bf16 ? launch_typed<128, true>(mq, mk, mv, p, grid, stream)
-               : launch_typed<128, false>(mq, mk, mv, p, grid, stream);
+      e = bf16 ? launch_typed<128, true>(mq, mk, mv, mo, p, grid, stream)
+               : launch_typed<128, false>(mq, mk, mv, mo, p, grid, stream);
     } else {
-      e = bf16 ? launch_typed<64, true>(mq, mk, mv, p, grid, stream)
-               : launch_typed<64, false>(mq, mk, mv, p, grid, stream);
+      e = bf16 ? launch_typed<64, true>(mq, mk, mv, mo, p, grid, stream)
+               : launch_typed<64, false>(mq, mk, mv, mo, p, grid, stream);
     }
   }
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -1387,6 +1428,7 @@ attn_status launch_attention_ulysses(const void* q, const void* k, const void* v
       !make_seq_map(&mk, k, bf16, D, H, Sl, R * B, box) ||
       !make_seq_map(&mv, v, bf16, D, H, Sl, R * B, box))
     return ATTN_ERR_CUDA;
+  const CUtensorMap& mo = mq;   // the sequence-sharded kernels store O directly
   int sms = device_sm_count();
   if (sms <= 0) return ATTN_ERR_CUDA;
   if (max_ctas > 0 && max_ctas < sms) sms = max_ctas;
@@ -1416,11 +1458,11 @@ attn_status launch_attention_ulysses(const void* q, const void* k, const void* v
   const int grid = p.num_units < sms ? p.num_units : sms;
   cudaError_t e;
   if (D == 128)
-    e = bf16 ? launch_typed<128, true, true>(mq, mk, mv, p, grid, stream)
-             : launch_typed<128, false, true>(mq, mk, mv, p, grid, stream);
+    e = bf16 ? launch_typed<128, true, true>(mq, mk, mv, mo, p, grid, stream)
+             : launch_typed<128, false, true>(mq, mk, mv, mo, p, grid, stream);
   else
-    e = bf16 ? launch_typed<64, true, true>(mq, mk, mv, p, grid, stream)
-             : launch_typed<64, false, true>(mq, mk, mv, p, grid, stream);
+    e = bf16 ? launch_typed<64, true, true>(mq, mk, mv, mo, p, grid, stream)
+             : launch_typed<64, false, true>(mq, mk, mv, mo, p, grid, stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -1451,9 +1493,9 @@ attn_status launch_attention_fp8(const void* q, const void* k, const void* vt, v
   int sms = device_sm_count();
   if (sms <= 0) return ATTN_ERR_CUDA;
   if (max_ctas > 0 && max_ctas < sms) sms = max_ctas;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!make_map_u8(&mq, q, D, Sq, BH) || !make_map_u8(&mk, k, D, Skv, BH) ||
-      !make_map_u8(&mv, vt, Skv, D, BH))
+      !make_map_u8(&mv, vt, Skv, D, BH) || !make_map(&mo, o, true, D, Sq, BH, 32))
     return ATTN_ERR_CUDA;
   Params p;
   p.Sq = Sq;
@@ -1473,7 +1515,7 @@ attn_status launch_attention_fp8(const void* q, const void* k, const void* vt, v
   p.lse = lse;
   p.limit_ns = limit_ns;
   const int grid = p.num_units < sms ? p.num_units : sms;
-  const cudaError_t e = launch_typed<D, true, false, true, true>(mq, mk, mv, p, grid, stream);
+  const cudaError_t e = launch_typed<D, true, false, true, true>(mq, mk, mv, mo, p, grid, stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
