@@ -82,7 +82,7 @@ CPATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, voi
  *   attn_lse_merge of these partials reproduces attn_fwd.  1 <= P <= Skv; other arguments as
  *   for attn_fwd.
  *   Short chunks cost throughput here: every chunk ends with a normalised partial output of
- *   the full query length (P times the bytes of O) and an accumulator drain, e.g. ~0.74 of the
+ *   the full query length (P times the bytes of O) and an accumulator drain, e.g. ~0.76 of the
  *   P = 1 rate at 576-key chunks.  When only the merged result is wanted, attn_fwd_ring
  *   computes it with the running state kept on chip across chunks (~0.84 of the P = 1 rate at
  *   576-key chunks, where the masked half tile at each chunk end is the remaining cost).
