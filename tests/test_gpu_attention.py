@@ -78,6 +78,23 @@ def test_small_shapes_sm_pair_kernel(B, H, Sq, Skv, D, dtype, P):
         cpattn.attn_set_kernel_variant(prev)
 
 
+@pytest.mark.parametrize("D", [128, 64])
+@pytest.mark.parametrize("tail", [1, 15, 16, 17, 63, 64, 65, 112, 127])
+def test_tail_tile_sizes(D, tail):
+    """KV lengths whose last 128-key tile holds `tail` valid keys: the S GEMM of that tile runs
+    with N rounded up to 16 and its P*V skips the all-masked 16-key steps.  Plain attention (one
+    chunk), two chunks of 128 + tail keys each through chunked + merge, and the ring."""
+    Skv = 256 + tail
+    q, k, v = rand_qkv(1, 2, 300, Skv, D, torch.bfloat16, seed=tail * 7 + D)
+    run_full_and_chunked(q, k, v, 1, f"tail {tail} D{D}")
+    q2, k2, v2 = rand_qkv(1, 2, 300, 2 * (128 + tail), D, torch.bfloat16, seed=tail * 11 + D)
+    run_full_and_chunked(q2, k2, v2, 2, f"2 chunks of 128 + {tail} D{D}")
+    orr, lrr = cpattn.attn_fwd_ring(q2.cuda(), k2.cuda(), v2.cuda(), 2)
+    assert cpattn.attn_device_status() == cpattn.ATTN_OK
+    o_ref, lse_ref = oracle.attention(q2, k2, v2)
+    assert_attention_close(orr, lrr, o_ref, lse_ref, f"ring, 2 chunks of 128 + {tail} D{D}")
+
+
 def test_pair_and_single_cta_kernels_agree():
     """D = 128: the CTA-pair and single-CTA kernels give the same result to rounding."""
     q, k, v = (t.cuda() for t in rand_qkv(1, 3, 1100, 900, 128, torch.bfloat16, seed=21))
