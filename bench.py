@@ -2,12 +2,13 @@
 
 One step = the ring-emulation hot path on the video-DiT workload (B=1, H=16, S=44,160, D=128,
 bf16): attn_fwd_chunked over P=8 KV chunks, then attn_lse_merge of the eight partials.  The
-metric is attention TFLOP/s = 4*B*H*Sq*Skv*D per step / step time.  Extra legs report the
-attention kernel alone against the tensor-core roofline (measured sustained and burst peaks, and
-the clock-derived nominal at the SM clock sampled during the timed region), the merge and Ulysses
-layout kernels in
-GB/s against HBM, an end-to-end number through the same API with host buffers, and the CPU
-oracle timed on a bounded sample.
+metric is attention TFLOP/s = 4*B*H*Sq*Skv*D per step / step time.  The roofline object holds
+the attention kernel alone against the measured burst dense-bf16 peak (with the sustained figure
+and the clock-derived nominal at the SM clock sampled during the timed region as notes) and its
+DRAM traffic from a full-size ncu capture.  Extra legs: the merge (L2 flushed) and Ulysses layout
+kernels in GB/s against HBM, the Ulysses, ring, e4m3 and short-chunk (image, P = 8) paths, an
+end-to-end number through the same API with host buffers, and the CPU oracle timed on a bounded
+sample.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
                     [--no-cpu-baseline] [--no-e2e]
