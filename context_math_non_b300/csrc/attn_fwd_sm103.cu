@@ -34,6 +34,11 @@
 // (and O rescaled) when it grows by more than 2^8, so most steps skip the rescale; the final
 // normalisation uses the same stale max, so results are exact.
 //
+// Shared memory: the two Q tiles, the K/V ring (4 stages of 32 KB at D = 128, 8 of 16 KB for
+// D = 64 and e4m3) and, for 16-bit outputs in the plain layout, one 4 KB output staging region
+// per softmax warp: a warp's 32 output rows leave through TMA stores instead of per-thread row
+// stores (see the epilogue).
+//
 // Every wait is bounded (see mbar_wait): a lost signal ends the kernel with ATTN_ERR_TIMEOUT in
 // the status word instead of a hang.
 
