@@ -1,6 +1,6 @@
 """GPU parity of the calls' options against the float64 oracle, through the C ABI: an explicit
-softmax scale in every attention entry point, outputs without LSE, and a problem with very many
-heads (thousands of units per launch)."""
+softmax scale in every attention entry point, outputs without LSE, a problem with very many heads
+(thousands of units per launch), and the chunked step replayed from a CUDA graph."""
 import numpy as np
 import pytest
 import torch
@@ -82,3 +82,33 @@ def test_many_heads():
     op_ref, lp_ref = oracle.attention_chunked(q, k, v, 2)
     assert_attention_close(o, lse, o_ref, lse_ref, "2048 heads")
     assert_attention_close(op, lp, op_ref, lp_ref, "2048 heads, chunked")
+
+
+def test_step_replays_from_a_cuda_graph():
+    """The chunked step (attn_fwd_chunked + attn_lse_merge) captured once in a CUDA graph and
+    replayed on new inputs written into the same buffers gives the bytes of direct calls."""
+    q, k, v = _qkv(1, 4, 700, 900, 128, torch.bfloat16, seed=61)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    op = torch.empty((3, 1, 4, 700, 128), dtype=torch.bfloat16, device="cuda")
+    lp = torch.empty((3, 1, 4, 700), dtype=torch.float32, device="cuda")
+    o = torch.empty_like(qd)
+    lse = torch.empty((1, 4, 700), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):          # warm-up outside the capture (one-time kernel set-up)
+        cpattn.attn_fwd_chunked(qd, kd, vd, 3, op, lp)
+        cpattn.attn_lse_merge(op, lp, o, lse)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        cpattn.attn_fwd_chunked(qd, kd, vd, 3, op, lp)
+        cpattn.attn_lse_merge(op, lp, o, lse)
+    q2, k2, v2 = _qkv(1, 4, 700, 900, 128, torch.bfloat16, seed=62)
+    qd.copy_(q2)
+    kd.copy_(k2)
+    vd.copy_(v2)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert cpattn.attn_device_status() == cpattn.ATTN_OK
+    o_ref, lse_ref = cpattn.attn_lse_merge(*cpattn.attn_fwd_chunked(q2.cuda(), k2.cuda(),
+                                                                  v2.cuda(), 3))
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
