@@ -227,6 +227,9 @@ def run_native(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     total_ms = t_start.elapsed_time(t_end)
+    # the timed step's merged output for its first query rows, checked by the CPU-baseline leg
+    check_rows = min(w.S, PARITY_ROWS)
+    gpu_head = (o[:, :, :check_rows].cpu(), lse[:, :, :check_rows].cpu())
     attn_ms = [e[0].elapsed_time(e[1]) for e in ev]
     merge_ms = [e[1].elapsed_time(e[2]) for e in ev]
     st = cpattn.attn_device_status(stream)
@@ -283,7 +286,9 @@ def run_native(args, rank, world, local_rank):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(q, k, v, budget_s=args.cpu_seconds)
+        cpu = cpu_baseline(q, k, v, budget_s=args.cpu_seconds, gpu_head=gpu_head)
+        if not cpu["parity"]["ok"]:
+            raise RuntimeError(f"the timed step's output fails the oracle check: {cpu['parity']}")
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -441,9 +446,31 @@ def _blas_threads() -> int:
     return os.cpu_count() or 1
 
 
-def cpu_baseline(q, k, v, budget_s: float = 15.0):
+PARITY_ROWS = 4096   # first query rows of every head copied back for the check
+
+
+def _parity(o_ref, lse_ref, gpu_head):
+    """The GPU step's merged O / LSE on the sampled rows against the oracle's: max and mean
+    |dO| and max |dLSE| with the bf16 attention bounds (1e-2 beyond half a bf16 spacing of the
+    exact value, 1e-3, 1e-3)."""
+    o_g, l_g = (t.double().numpy() for t in gpu_head)
+    n = min(o_ref.shape[-2], o_g.shape[-2])
+    o_r, l_r = o_ref[..., :n, :], lse_ref[..., :n]
+    o_g, l_g = o_g[..., :n, :], l_g[..., :n]
+    err = np.abs(o_g - o_r)
+    half = np.exp2(np.floor(np.log2(np.maximum(np.abs(o_r), 2.0 ** -126))) - 8)
+    out = {"rows_per_head": int(n), "max_abs": float(err.max()), "mean_abs": float(err.mean()),
+           "lse_max_abs": float(np.abs(l_g - l_r).max())}
+    out["ok"] = bool((err - half).max() <= 1e-2 and out["mean_abs"] <= 1e-3 and
+                     out["lse_max_abs"] <= 1e-3)
+    return out
+
+
+def cpu_baseline(q, k, v, budget_s: float = 15.0, gpu_head=None):
     """The float64 oracle, as it stands, timed on this host on a bounded sample of the same
-    workload: R query rows of every head through chunked attention (P=8) and the merge."""
+    workload: R query rows of every head through chunked attention (P=8) and the merge.  With
+    gpu_head (the timed step's O and LSE for the first rows of every head) the same oracle
+    output also checks the GPU result on those rows."""
     w = WORKLOAD
     _oracle_sample(q, k, v, 16, 1)                  # warm BLAS and the allocator
     rows = 32
@@ -457,10 +484,11 @@ def cpu_baseline(q, k, v, budget_s: float = 15.0):
     per_row = t_cal / rows
     rows = int(max(16, min(w.S, budget_s / per_row / w.H)))
     t0 = time.perf_counter()
-    _oracle_sample(q, k, v, rows, w.H)
+    o_ref, lse_ref = _oracle_sample(q, k, v, rows, w.H)
     dt = time.perf_counter() - t0
     flops = 4.0 * w.B * w.H * rows * w.S * w.D
     return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": _blas_threads(),
+            "parity": None if gpu_head is None else _parity(o_ref, lse_ref, gpu_head),
             "kind": "oracle", "seconds": round(dt, 2),
             "extrapolated_full_seconds": round(dt * w.S / rows, 1),
             "sample": f"first {rows} query rows of each of the {w.H} heads (of {w.S}), full KV, "
