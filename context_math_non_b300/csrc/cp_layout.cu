@@ -27,6 +27,9 @@ namespace {
 constexpr int kLayoutThreads = 256;
 constexpr int kUnroll = 4;
 constexpr bool kSeq2HeadWalksHead = true;   // seq2head walks its destination (head-sharded) space
+// Tiled kernel: adjacent heads a block moves together (their rows are contiguous in the
+// sequence-sharded layout); the largest power of two up to this that divides H/P is used.
+constexpr int kLayoutHeads = 4;
 
 // kHeadLinear: threads walk the head-sharded index space linearly (true) or the sequence-sharded
 // one (false); the other side is then accessed in runs of one (token, head) row.
@@ -98,27 +101,35 @@ __global__ void __launch_bounds__(kLayoutThreads)
 template <bool kSeq2Head>
 __global__ void __launch_bounds__(kLayoutThreads)
     layout_tile_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, int B, int Hl, int S,
-                       int Sl, int H, int vpr_log2, int nsb) {
-  const int gbj = blockIdx.y;                   // (g * B + b) * Hl + j
-  const int j = gbj % Hl;
-  const int gb = gbj / Hl;
+                       int Sl, int H, int vpr_log2, int hb_log2, int nsb) {
+  // block: rank p, token run sb, and heads j0 .. j0 + 2^hb_log2 - 1 of rank g, batch b
+  const int Hg = Hl >> hb_log2;                 // head groups per (rank, batch)
+  const int gbjg = blockIdx.y;                  // (g * B + b) * Hg + jg
+  const int jg = gbjg % Hg;
+  const int gb = gbjg / Hg;
   const int b = gb % B;
   const int g = gb / B;
+  const int j0 = jg << hb_log2;
   const int p = blockIdx.x / nsb;
   const int sb = blockIdx.x - p * nsb;
-  const int rows = kLayoutThreads >> vpr_log2;  // token rows per pass of the block
-  const int x = threadIdx.x & ((1 << vpr_log2) - 1);
-  const int rl = threadIdx.x >> vpr_log2;
-  // row indices of token s = 0 of this (rank, head) on both sides
-  const long long seq_row0 = static_cast<long long>(p * B + b) * Sl * H + g * Hl + j;
-  const long long head_row0 = static_cast<long long>(gbj) * S + static_cast<long long>(p) * Sl;
+  const int c_log2 = vpr_log2 + hb_log2;        // vectors of one token over the block's heads
+  const int rows = kLayoutThreads >> c_log2;    // token rows per pass of the block
+  const int c = threadIdx.x & ((1 << c_log2) - 1);
+  const int rl = threadIdx.x >> c_log2;
+  const int jj = c >> vpr_log2;                 // head of the group this thread moves
+  const int x = c & ((1 << vpr_log2) - 1);
+  // row indices of token s = 0 on both sides: the sequence-sharded side starts at the group's
+  // first head (the group's rows are contiguous there), the head-sharded side at this head
+  const long long seq_row0 = static_cast<long long>(p * B + b) * Sl * H + g * Hl + j0;
+  const long long head_row0 = static_cast<long long>(gb * Hl + j0 + jj) * S +
+                              static_cast<long long>(p) * Sl;
   uint4 v[kUnroll];
   long long dst[kUnroll];
 #pragma unroll
   for (int u = 0; u < kUnroll; ++u) {
     const int s = (sb * kUnroll + u) * rows + rl;
     if (s < Sl) {
-      const long long seq_i = ((seq_row0 + static_cast<long long>(s) * H) << vpr_log2) + x;
+      const long long seq_i = ((seq_row0 + static_cast<long long>(s) * H) << vpr_log2) + c;
       const long long head_i = ((head_row0 + s) << vpr_log2) + x;
       v[u] = __ldcs(in + (kSeq2Head ? seq_i : head_i));
       dst[u] = kSeq2Head ? head_i : seq_i;
@@ -164,18 +175,24 @@ attn_status launch_layout(const void* in, void* out, int P, int B, int S, int H,
   cudaError_t e;
   int vpr_log2 = 0;
   while ((1 << vpr_log2) < vpr) ++vpr_log2;
-  const long long heads = static_cast<long long>(P) * B * Hl;
+  int hb_log2 = 0;
+  while ((2 << hb_log2) <= kLayoutHeads && Hl % (2 << hb_log2) == 0 &&
+         (vpr << (hb_log2 + 1)) <= kLayoutThreads)
+    ++hb_log2;
+  const long long heads = (static_cast<long long>(P) * B * Hl) >> hb_log2;   // head groups
   if ((1 << vpr_log2) == vpr && vpr <= kLayoutThreads && heads <= 65535) {
-    const int tokens_per_block = kUnroll * (kLayoutThreads / vpr);
+    const int tokens_per_block = kUnroll * (kLayoutThreads / (vpr << hb_log2));
     const int nsb = (Sl + tokens_per_block - 1) / tokens_per_block;
     const dim3 grid(static_cast<unsigned>(static_cast<long long>(P) * nsb),
                     static_cast<unsigned>(heads));
     if (seq2head)
       layout_tile_kernel<true><<<grid, kLayoutThreads, 0, stream>>>(
-          static_cast<const uint4*>(in), static_cast<uint4*>(out), B, Hl, S, Sl, H, vpr_log2, nsb);
+          static_cast<const uint4*>(in), static_cast<uint4*>(out), B, Hl, S, Sl, H, vpr_log2, hb_log2,
+          nsb);
     else
       layout_tile_kernel<false><<<grid, kLayoutThreads, 0, stream>>>(
-          static_cast<const uint4*>(in), static_cast<uint4*>(out), B, Hl, S, Sl, H, vpr_log2, nsb);
+          static_cast<const uint4*>(in), static_cast<uint4*>(out), B, Hl, S, Sl, H, vpr_log2, hb_log2,
+          nsb);
     e = cudaGetLastError();
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
   }
